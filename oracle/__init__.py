@@ -1,0 +1,187 @@
+"""fp64 CPU oracle for block-causal / staircase attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this package; the product library and its Python
+binding never do.  It shares no code with the CUDA path.
+
+`oracle.c` holds the plain definition (explicit mask, dense rows, fp64); this
+module marshals numpy/torch inputs into it, one packed sequence at a time.
+`brute.py` holds an independent NumPy brute force for tiny inputs.
+
+Mask kinds follow the ORL announcement thread (24vids.com mirror),
+highlight 3 (block-causal) and Insight 3 (staircase), and the ORL paper card
+(thelatestinai.com), Figure 3 caption.  Every array is THD:
+Q/O/dO/dQ [T_q][Hq][d], K/V/dK/dV [T_k][Hkv][d], LSE [Hq][T_q].
+
+Parity unpinned: none -- every function here is pinned by tests/test_oracle_*.py.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+BLOCK_CAUSAL = 0
+STAIRCASE = 1
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        c_int, c_dbl = ctypes.c_int, ctypes.c_double
+        pd = ctypes.POINTER(ctypes.c_double)
+        pi = ctypes.POINTER(ctypes.c_int32)
+        lib.oracle_allowed.argtypes = [c_int] * 7
+        lib.oracle_allowed.restype = c_int
+        lib.oracle_mask.argtypes = [c_int] * 5 + [ctypes.POINTER(ctypes.c_uint8)]
+        lib.oracle_mask.restype = None
+        lib.oracle_count_pairs.argtypes = [c_int] * 5
+        lib.oracle_count_pairs.restype = ctypes.c_longlong
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = c_int
+        lib.oracle_fwd_seq.argtypes = ([c_int] * 8 + [c_dbl, pd, pd, pd, c_int, c_int, pi, c_int,
+                                                     pd, pd])
+        lib.oracle_fwd_seq.restype = None
+        lib.oracle_bwd_seq.argtypes = ([c_int] * 8 + [c_dbl, pd, pd, pd, pd, c_int, c_int, pi,
+                                                     c_int, pi, c_int, pd, pd, pd])
+        lib.oracle_bwd_seq.restype = None
+        _lib = lib
+    return _lib
+
+
+def _f64(x):
+    """Any array-like (numpy, torch CPU of any float dtype) -> C-contiguous fp64."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _rows(rows):
+    if rows is None:
+        return None, 0
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    return r, int(r.size)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def allowed(kind, B, P, Lq, Lk, i, j) -> bool:
+    return bool(_load().oracle_allowed(kind, B, P, Lq, Lk, i, j))
+
+
+def mask(kind, B, P, Lq, Lk) -> np.ndarray:
+    m = np.zeros((Lq, Lk), dtype=np.uint8)
+    _load().oracle_mask(kind, B, P, Lq, Lk, _ptr(m, ctypes.c_uint8))
+    return m.astype(bool)
+
+
+def count_pairs(kind, B, P, Lq, Lk) -> int:
+    return int(_load().oracle_count_pairs(kind, B, P, Lq, Lk))
+
+
+def _prefix(kind, prefix, s, Lk):
+    if kind == STAIRCASE:
+        return int(prefix[s])
+    return Lk  # unused by the block-causal predicate
+
+
+def fwd_seq(kind, B, P, Q, K, V, hq, hkv, scale, heads=None, rows=None):
+    """One sequence.  Q [Lq][Hq][d], K/V [Lk][Hkv][d] (any float type).
+    Returns (O [n][Hq][d], LSE [Hq][n]) in fp64, n = Lq or len(rows); heads
+    outside `heads` = (lo, hi) are left NaN."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    Lq, Lk, d = Q.shape[0], K.shape[0], Q.shape[2]
+    h_lo, h_hi = heads if heads is not None else (0, hq)
+    r, nr = _rows(rows)
+    n = Lq if r is None else nr
+    O = np.full((n, hq, d), np.nan)
+    LSE = np.full((hq, n), np.nan)
+    _load().oracle_fwd_seq(kind, B, P, Lq, Lk, hq, hkv, d, scale, _ptr(Q), _ptr(K), _ptr(V),
+                           h_lo, h_hi, None if r is None else _ptr(r, ctypes.c_int32), n,
+                           _ptr(O), _ptr(LSE))
+    return O, LSE
+
+
+def bwd_seq(kind, B, P, Q, K, V, dO, hq, hkv, scale, kv_heads=None, qrows=None, krows=None):
+    """One sequence.  Returns (dQ [nq][Hq][d], dK [nk][Hkv][d], dV [nk][Hkv][d]),
+    fp64; entries of heads outside `kv_heads` = (lo, hi) are left NaN."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    Lq, Lk, d = Q.shape[0], K.shape[0], Q.shape[2]
+    lo, hi = kv_heads if kv_heads is not None else (0, hkv)
+    qr, nq = _rows(qrows)
+    kr, nk = _rows(krows)
+    nq = Lq if qr is None else nq
+    nk = Lk if kr is None else nk
+    dQ = np.full((nq, hq, d), np.nan)
+    dK = np.full((nk, hkv, d), np.nan)
+    dV = np.full((nk, hkv, d), np.nan)
+    _load().oracle_bwd_seq(kind, B, P, Lq, Lk, hq, hkv, d, scale, _ptr(Q), _ptr(K), _ptr(V),
+                           _ptr(dO), lo, hi, None if qr is None else _ptr(qr, ctypes.c_int32), nq,
+                           None if kr is None else _ptr(kr, ctypes.c_int32), nk, _ptr(dQ),
+                           _ptr(dK), _ptr(dV))
+    return dQ, dK, dV
+
+
+def fwd(kind, B, cu_q, cu_k, prefix, Q, K, V, hq, hkv, scale, heads=None):
+    """Packed varlen forward: cu_q/cu_k int [nseq+1]; prefix [nseq] (staircase)
+    or None.  Returns (O [T_q][Hq][d], LSE [Hq][T_q]) fp64."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    cu_q = [int(x) for x in cu_q]
+    cu_k = [int(x) for x in cu_k]
+    Tq, d = Q.shape[0], Q.shape[2]
+    O = np.full((Tq, hq, d), np.nan)
+    LSE = np.full((hq, Tq), np.nan)
+    for s in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
+        if q1 == q0:
+            continue
+        P = _prefix(kind, prefix, s, k1 - k0)
+        o, l = fwd_seq(kind, B, P, Q[q0:q1], K[k0:k1], V[k0:k1], hq, hkv, scale, heads)
+        O[q0:q1] = o
+        LSE[:, q0:q1] = l
+    return O, LSE
+
+
+def bwd(kind, B, cu_q, cu_k, prefix, Q, K, V, dO, hq, hkv, scale, kv_heads=None):
+    """Packed varlen backward.  Returns (dQ, dK, dV) fp64 in THD layout."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    cu_q = [int(x) for x in cu_q]
+    cu_k = [int(x) for x in cu_k]
+    dQ = np.full(Q.shape, np.nan)
+    dK = np.full(K.shape, np.nan)
+    dV = np.full(V.shape, np.nan)
+    for s in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
+        if k1 == k0:
+            continue
+        P = _prefix(kind, prefix, s, k1 - k0)
+        if q1 == q0:
+            dK[k0:k1] = 0.0
+            dV[k0:k1] = 0.0
+            continue
+        dq, dk, dv = bwd_seq(kind, B, P, Q[q0:q1], K[k0:k1], V[k0:k1], dO[q0:q1], hq, hkv,
+                             scale, kv_heads)
+        dQ[q0:q1] = dq
+        dK[k0:k1] = dk
+        dV[k0:k1] = dv
+    return dQ, dK, dV
+
+
+def count_pairs_packed(kind, B, cu_q, cu_k, prefix) -> int:
+    """Allowed (i, j) pairs summed over the packed sequences (per head)."""
+    n = 0
+    for s in range(len(cu_q) - 1):
+        Lq, Lk = int(cu_q[s + 1] - cu_q[s]), int(cu_k[s + 1] - cu_k[s])
+        n += count_pairs(kind, B, _prefix(kind, prefix, s, Lk), Lq, Lk)
+    return n

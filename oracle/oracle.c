@@ -1,0 +1,273 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for block-causal and staircase attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this code.  It shares nothing
+ * with the CUDA path (no headers, no helpers, no tables) and is never called
+ * by the product library.
+ *
+ * What it computes (the plain definition, no tiling, no online softmax):
+ *   - ORL announcement thread (24vids.com mirror), highlight 3: attention for
+ *     block-diffusion LMs is *block-causal*: a sequence is cut into blocks of
+ *     B tokens; a query sees every key of its own block (bidirectionally) and
+ *     every key of all earlier blocks.
+ *   - Same thread, Insight 3, and ORL paper card (thelatestinai.com),
+ *     Figure 3 caption: training replays packed trajectories with a
+ *     *staircase* kernel: after a clean prefix of P tokens sit K copies of
+ *     the active block (one per denoising step); every copy sees the prefix
+ *     and itself only.
+ *   - The attention itself is ordinary scaled-dot-product softmax attention
+ *     (the thread compares it with FlashAttention), with the natural-log
+ *     log-sum-exp of each query row kept for the backward pass, and the
+ *     textbook softmax-attention gradients.
+ *
+ * Readings taken where the pages are silent (each one listed in the design
+ * notes of the repository):
+ *   - staircase prefix rows are queries too and are block-causal inside the
+ *     prefix (block size = copy length); they never see copies;
+ *   - when a sequence has fewer queries than keys (a decode step), query row i
+ *     sits at key position p = i + (Lk - Lq) (aligned to the end);
+ *   - GQA: query head h reads KV head floor(h / G), G = Hq / Hkv;
+ *   - LSE is the natural logarithm.
+ *
+ * Layout of every array handed in (one sequence at a time, row-major fp64):
+ *   Q, dO, O, dQ : [Lq][Hq][d]     K, V, dK, dV : [Lk][Hkv][d]
+ *   LSE          : [Hq][Lq]
+ *
+ * The parallel loops only split independent rows / columns across threads;
+ * each row is still computed by the plain definition.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_BLOCK_CAUSAL 0
+#define ORACLE_STAIRCASE 1
+
+/* allowed(i, j): may local query row i attend to local key j?
+ * Block-causal (announcement thread, highlight 3):
+ *     floor(j / B) <= floor(p / B),                p = i + (Lk - Lq).
+ * Staircase (announcement thread, Insight 3; paper card, Figure 3):
+ *     row in the prefix (p < P):  j < P  and  floor(j / B) <= floor(p / B)
+ *     row in copy c = floor((p - P) / B):  j < P  or  floor((j - P) / B) == c */
+int oracle_allowed(int kind, int B, int P, int Lq, int Lk, int i, int j)
+{
+    if (i < 0 || i >= Lq || j < 0 || j >= Lk || B <= 0) return 0;
+    long p = (long)i + (long)(Lk - Lq);
+    if (kind == ORACLE_BLOCK_CAUSAL) return (j / B) <= (p / B);
+    if (p < P) return j < P && (j / B) <= (p / B);
+    if (j < P) return 1;
+    return ((long)j - P) / B == (p - P) / B;
+}
+
+/* The explicit mask of one sequence, M[i*Lk + j] in {0,1}. */
+void oracle_mask(int kind, int B, int P, int Lq, int Lk, uint8_t *M)
+{
+    for (int i = 0; i < Lq; ++i)
+        for (int j = 0; j < Lk; ++j)
+            M[(size_t)i * Lk + j] = (uint8_t)oracle_allowed(kind, B, P, Lq, Lk, i, j);
+}
+
+/* Number of allowed (i, j) pairs of one sequence (per head). */
+long long oracle_count_pairs(int kind, int B, int P, int Lq, int Lk)
+{
+    long long n = 0;
+    for (int i = 0; i < Lq; ++i)
+        for (int j = 0; j < Lk; ++j)
+            n += oracle_allowed(kind, B, P, Lq, Lk, i, j);
+    return n;
+}
+
+static int max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+int oracle_num_threads(void) { return max_threads(); }
+
+/* One query row of one head: fill mrow (mask row), S (scores, -inf where
+ * masked), P (probabilities), and return LSE.  O row (d values) written. */
+static double row_forward(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int d,
+                          double scale, const double *Q, const double *K, const double *V,
+                          int h, int i, uint8_t *mrow, double *S, double *Pr, double *Orow)
+{
+    const int G = Hq / Hkv;
+    const int kvh = h / G;
+    const double *q = Q + ((size_t)i * Hq + h) * d;
+    for (int j = 0; j < Lk; ++j) mrow[j] = (uint8_t)oracle_allowed(kind, B, P, Lq, Lk, i, j);
+    /* S_ij = scale * <Q_i, K_j>, -inf where not allowed */
+    double m = -INFINITY;
+    for (int j = 0; j < Lk; ++j) {
+        if (!mrow[j]) { S[j] = -INFINITY; continue; }
+        const double *k = K + ((size_t)j * Hkv + kvh) * d;
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += q[c] * k[c];
+        S[j] = scale * acc;
+        if (S[j] > m) m = S[j];
+    }
+    /* P = softmax_j(S); LSE = ln sum_j exp(S_ij) */
+    double Z = 0.0;
+    for (int j = 0; j < Lk; ++j) {
+        Pr[j] = mrow[j] ? exp(S[j] - m) : 0.0;
+        Z += Pr[j];
+    }
+    for (int j = 0; j < Lk; ++j) Pr[j] /= Z;
+    /* O_i = sum_j P_ij V_j */
+    for (int c = 0; c < d; ++c) Orow[c] = 0.0;
+    for (int j = 0; j < Lk; ++j) {
+        if (!mrow[j]) continue;
+        const double *v = V + ((size_t)j * Hkv + kvh) * d;
+        for (int c = 0; c < d; ++c) Orow[c] += Pr[j] * v[c];
+    }
+    return m + log(Z);
+}
+
+/* Forward for one sequence, query heads [h_lo, h_hi).  rows == NULL: every
+ * row, outputs indexed by row; else only rows[0..nrows), outputs indexed by
+ * position in that list (O: [nrows][Hq][d], LSE: [Hq][nrows]). */
+void oracle_fwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int d, double scale,
+                    const double *Q, const double *K, const double *V, int h_lo, int h_hi,
+                    const int32_t *rows, int nrows, double *O, double *LSE)
+{
+    const int nr = rows ? nrows : Lq;
+    const long ntask = (long)(h_hi - h_lo) * nr;
+#pragma omp parallel
+    {
+        uint8_t *mrow = (uint8_t *)malloc((size_t)Lk + 1);
+        double *S = (double *)malloc(sizeof(double) * ((size_t)Lk + 1));
+        double *Pr = (double *)malloc(sizeof(double) * ((size_t)Lk + 1));
+#pragma omp for schedule(dynamic, 4)
+        for (long t = 0; t < ntask; ++t) {
+            const int h = h_lo + (int)(t / nr);
+            const int r = (int)(t % nr);
+            const int i = rows ? rows[r] : r;
+            double *Orow = O + ((size_t)r * Hq + h) * d;
+            LSE[(size_t)h * nr + r] = row_forward(kind, B, P, Lq, Lk, Hq, Hkv, d, scale, Q, K, V,
+                                                  h, i, mrow, S, Pr, Orow);
+        }
+        free(mrow);
+        free(S);
+        free(Pr);
+    }
+}
+
+/* Backward for one sequence, KV heads [kvh_lo, kvh_hi) (and their G query
+ * heads).  Textbook softmax-attention gradients:
+ *   dV = P^T dO;  dP = dO V^T;  D_i = sum_c dO_ic O_ic;  dS = P o (dP - D);
+ *   dQ = scale dS K;  dK = scale dS^T Q;  dK, dV summed over the G query
+ *   heads that share a KV head.
+ * qrows (or NULL = all Lq rows) selects the dQ rows computed; dQ indexed by
+ * position in that list: [nq][Hq][d].  krows (or NULL = all Lk keys) selects
+ * the dK/dV rows computed: [nk][Hkv][d].  Only heads in range are written.
+ * P_ij for a key column is exp(S_ij - LSE_i), the same softmax. */
+void oracle_bwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int d, double scale,
+                    const double *Q, const double *K, const double *V, const double *dO,
+                    int kvh_lo, int kvh_hi, const int32_t *qrows, int nq, const int32_t *krows,
+                    int nk, double *dQ, double *dK, double *dV)
+{
+    const int G = Hq / Hkv;
+    const int h_lo = kvh_lo * G, h_hi = kvh_hi * G;
+    const int nqr = qrows ? nq : Lq;
+    const int nkr = krows ? nk : Lk;
+
+    /* Which query rows are needed: the dQ rows, and every row that sees one of
+     * the requested keys. */
+    uint8_t *need = (uint8_t *)calloc((size_t)Lq + 1, 1);
+    for (int r = 0; r < nqr; ++r) need[qrows ? qrows[r] : r] = 1;
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < Lq; ++i) {
+        if (need[i]) continue;
+        for (int r = 0; r < nkr; ++r)
+            if (oracle_allowed(kind, B, P, Lq, Lk, i, krows ? krows[r] : r)) { need[i] = 1; break; }
+    }
+    int32_t *qpos = (int32_t *)malloc(sizeof(int32_t) * ((size_t)Lq + 1));
+    for (int i = 0; i < Lq; ++i) qpos[i] = -1;
+    if (qrows)
+        for (int r = 0; r < nq; ++r) qpos[qrows[r]] = r;
+    else
+        for (int i = 0; i < Lq; ++i) qpos[i] = i;
+
+    /* Per needed row and head: LSE_i, D_i, and (for dQ rows) dQ_i. */
+    double *LSE = (double *)malloc(sizeof(double) * ((size_t)Lq * Hq + 1));
+    double *Dv = (double *)malloc(sizeof(double) * ((size_t)Lq * Hq + 1));
+    const long ntask = (long)(h_hi - h_lo) * Lq;
+#pragma omp parallel
+    {
+        uint8_t *mrow = (uint8_t *)malloc((size_t)Lk + 1);
+        double *S = (double *)malloc(sizeof(double) * ((size_t)Lk + 1));
+        double *Pr = (double *)malloc(sizeof(double) * ((size_t)Lk + 1));
+        double *Orow = (double *)malloc(sizeof(double) * ((size_t)d + 1));
+#pragma omp for schedule(dynamic, 4)
+        for (long t = 0; t < ntask; ++t) {
+            const int h = h_lo + (int)(t / Lq);
+            const int i = (int)(t % Lq);
+            if (!need[i]) continue;
+            const int kvh = h / G;
+            const double lse = row_forward(kind, B, P, Lq, Lk, Hq, Hkv, d, scale, Q, K, V, h, i,
+                                           mrow, S, Pr, Orow);
+            const double *dout = dO + ((size_t)i * Hq + h) * d;
+            double D = 0.0;
+            for (int c = 0; c < d; ++c) D += dout[c] * Orow[c];
+            LSE[(size_t)i * Hq + h] = lse;
+            Dv[(size_t)i * Hq + h] = D;
+            if (qpos[i] < 0) continue;
+            double *dq = dQ + ((size_t)qpos[i] * Hq + h) * d;
+            for (int c = 0; c < d; ++c) dq[c] = 0.0;
+            for (int j = 0; j < Lk; ++j) {
+                if (!mrow[j]) continue;
+                const double *v = V + ((size_t)j * Hkv + kvh) * d;
+                const double *k = K + ((size_t)j * Hkv + kvh) * d;
+                double dp = 0.0;
+                for (int c = 0; c < d; ++c) dp += dout[c] * v[c];
+                const double ds = Pr[j] * (dp - D);
+                for (int c = 0; c < d; ++c) dq[c] += scale * ds * k[c];
+            }
+        }
+        free(mrow);
+        free(S);
+        free(Pr);
+        free(Orow);
+    }
+
+    /* Per requested key and KV head: dK_j, dV_j over every row and head of
+     * the group that sees key j. */
+    const long ktask = (long)(kvh_hi - kvh_lo) * nkr;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long t = 0; t < ktask; ++t) {
+        const int kvh = kvh_lo + (int)(t / nkr);
+        const int r = (int)(t % nkr);
+        const int j = krows ? krows[r] : r;
+        double *dk = dK + ((size_t)r * Hkv + kvh) * d;
+        double *dv = dV + ((size_t)r * Hkv + kvh) * d;
+        for (int c = 0; c < d; ++c) { dk[c] = 0.0; dv[c] = 0.0; }
+        const double *k = K + ((size_t)j * Hkv + kvh) * d;
+        const double *v = V + ((size_t)j * Hkv + kvh) * d;
+        for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
+            for (int i = 0; i < Lq; ++i) {
+                if (!oracle_allowed(kind, B, P, Lq, Lk, i, j)) continue;
+                const double *q = Q + ((size_t)i * Hq + h) * d;
+                const double *dout = dO + ((size_t)i * Hq + h) * d;
+                double s = 0.0, dp = 0.0;
+                for (int c = 0; c < d; ++c) { s += q[c] * k[c]; dp += dout[c] * v[c]; }
+                const double p = exp(scale * s - LSE[(size_t)i * Hq + h]);
+                const double ds = p * (dp - Dv[(size_t)i * Hq + h]);
+                for (int c = 0; c < d; ++c) {
+                    dv[c] += p * dout[c];
+                    dk[c] += scale * ds * q[c];
+                }
+            }
+        }
+    }
+    free(need);
+    free(qpos);
+    free(LSE);
+    free(Dv);
+}
