@@ -1,0 +1,288 @@
+// bda_api.cu -- the extern "C" entry points declared in include/bda_attn.h.
+//
+// Host side of every call: validate the problem (nothing is launched on an
+// argument error), encode the TMA tensor maps over the caller's THD tensors,
+// and launch the kernels on the caller's stream.  No device memory is
+// allocated here; scratch lives in the caller's workspace.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/bda_attn.h"
+#include "bda_host.h"
+#include "bda_internal.h"
+#include "bda_kernels.h"
+
+namespace bda {
+namespace {
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 3-D map over a THD bf16 tensor [rows][heads][d]; box = 64 head-dim elements
+// (128 bytes, 128B swizzle) x box_h heads x box_rows rows.
+bool make_thd_map(CUtensorMap* m, const void* ptr, int d, int heads, int64_t rows, int box_h,
+                  int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
+  cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(d) * 2 * cuuint64_t(heads)};
+  cuuint32_t box[3] = {64, cuuint32_t(box_h), cuuint32_t(box_rows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bda_status check_ws(const Shape& s, const void* ws, size_t ws_bytes, bool with_bwd) {
+  if (!ws || !aligned16(ws)) return BDA_ERR_INVALID_ARG;
+  if (ws_bytes < workspace_bytes(s, with_bwd)) return BDA_ERR_WORKSPACE;
+  return BDA_OK;
+}
+
+thread_local const char* g_last_cuda_error = "";
+
+bda_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return BDA_OK;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return BDA_ERR_CUDA;
+}
+
+bda_status tensor_map_error() {
+  g_last_cuda_error = "cuTensorMapEncodeTiled failed";
+  return BDA_ERR_CUDA;
+}
+
+const uint8_t* plan_ptr(const void* ws) { return static_cast<const uint8_t*>(ws); }
+
+}  // namespace
+}  // namespace bda
+
+using namespace bda;
+
+extern "C" {
+
+size_t bda_attn_plan_size(const bda_problem* prob, const bda_mask_desc* mask) {
+  Shape s;
+  if (validate(prob, mask, &s) != BDA_OK) return 0;
+  return plan_bytes(s);
+}
+
+size_t bda_attn_workspace_size(const bda_problem* prob, const bda_mask_desc* mask, int with_bwd) {
+  Shape s;
+  if (validate(prob, mask, &s) != BDA_OK) return 0;
+  return workspace_bytes(s, with_bwd != 0);
+}
+
+long long bda_attn_count_pairs(const bda_problem* prob, const bda_mask_desc* mask) {
+  Shape s;
+  if (validate(prob, mask, &s) != BDA_OK) return -1;
+  return count_pairs(prob, mask, s);
+}
+
+bda_status bda_attn_plan_host(const bda_problem* prob, const bda_mask_desc* mask, void* host_plan,
+                              size_t host_plan_bytes) {
+  Shape s;
+  bda_status st = validate(prob, mask, &s);
+  if (st != BDA_OK) return st;
+  if (!host_plan) return BDA_ERR_INVALID_ARG;
+  if (host_plan_bytes < plan_bytes(s)) return BDA_ERR_WORKSPACE;
+  build_plan(prob, mask, s, static_cast<uint8_t*>(host_plan));
+  return BDA_OK;
+}
+
+bda_status bda_attn_plan(const bda_problem* prob, const bda_mask_desc* mask, void* host_plan,
+                         size_t host_plan_bytes, void* ws, size_t ws_bytes, bda_stream_t stream) {
+  Shape s;
+  bda_status st = validate(prob, mask, &s);
+  if (st != BDA_OK) return st;
+  if (!host_plan) return BDA_ERR_INVALID_ARG;
+  if (host_plan_bytes < plan_bytes(s)) return BDA_ERR_WORKSPACE;
+  if ((st = check_ws(s, ws, ws_bytes, false)) != BDA_OK) return st;
+  build_plan(prob, mask, s, static_cast<uint8_t*>(host_plan));
+  return cuda_status(cudaMemcpyAsync(ws, host_plan, plan_bytes(s), cudaMemcpyHostToDevice,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bda_status bda_attn_fwd(const bda_problem* prob, const bda_mask_desc* mask, const void* q,
+                        const void* k, const void* v, void* o, float* lse, void* ws,
+                        size_t ws_bytes, bda_stream_t stream) {
+  Shape s;
+  bda_status st = validate(prob, mask, &s);
+  if (st != BDA_OK) return st;
+  if ((st = check_ws(s, ws, ws_bytes, false)) != BDA_OK) return st;
+  if (s.n_fwd == 0) return BDA_OK;
+  if (!q || !k || !v || !o || !lse) return BDA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return BDA_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv;
+  if (!make_thd_map(&tq, q, s.d, s.hq, s.total_q, s.hg, s.tok) ||
+      !make_thd_map(&tk, k, s.d, s.hkv, s.total_k, 1, kTileN) ||
+      !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN))
+    return tensor_map_error();
+  FwdArgs a{};
+  a.items = reinterpret_cast<const FwdItem*>(plan_ptr(ws) + kHeaderBytes);
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.timeout_ns = kTimeoutNs;
+  a.n_groups = s.hq / s.hg;
+  a.hg = s.hg;
+  a.lg_hg = s.lg_hg;
+  a.G = s.G;
+  a.hq = s.hq;
+  a.total_q = int(s.total_q);
+  a.block = s.B;
+  a.scale_log2 = s.scale * 1.4426950408889634f;
+  return cuda_status(launch_fwd(s.d, tq, tk, tv, a, s.n_fwd, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bda_status bda_attn_bwd_preprocess(const bda_problem* prob, const bda_mask_desc* mask,
+                                   const void* o, const void* dout, void* ws, size_t ws_bytes,
+                                   bda_stream_t stream) {
+  Shape s;
+  bda_status st = validate(prob, mask, &s);
+  if (st != BDA_OK) return st;
+  if ((st = check_ws(s, ws, ws_bytes, true)) != BDA_OK) return st;
+  if (s.total_q == 0) return BDA_OK;
+  if (!o || !dout || !aligned16(o) || !aligned16(dout)) return BDA_ERR_INVALID_ARG;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  return cuda_status(launch_bwd_preprocess(
+      s.d, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
+      reinterpret_cast<float*>(w + ws_offset_D(s)), reinterpret_cast<float*>(w + ws_offset_dqacc(s)),
+      s.total_q, s.hq, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bda_status bda_attn_bwd_dkdv(const bda_problem* prob, const bda_mask_desc* mask, const void* q,
+                             const void* k, const void* v, const float* lse, const void* dout,
+                             void* dk, void* dv, void* ws, size_t ws_bytes, bda_stream_t stream) {
+  Shape s;
+  bda_status st = validate(prob, mask, &s);
+  if (st != BDA_OK) return st;
+  if ((st = check_ws(s, ws, ws_bytes, true)) != BDA_OK) return st;
+  if (s.n_bwd == 0) return BDA_OK;
+  if (!k || !v || !dk || !dv) return BDA_ERR_INVALID_ARG;
+  if (s.total_q > 0 && (!q || !lse || !dout)) return BDA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dk) || !aligned16(dv))
+    return BDA_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv, tdo;
+  // A problem without queries still launches (dK = dV = 0); point the query
+  // maps at the key tensor, they are never read.
+  const int64_t rq = s.total_q > 0 ? s.total_q : 1;
+  const void* qsrc = s.total_q > 0 ? q : k;
+  const void* dsrc = s.total_q > 0 ? dout : k;
+  const int hq_map = s.total_q > 0 ? s.hq : s.hkv;
+  if (!make_thd_map(&tq, qsrc, s.d, hq_map, rq, s.total_q > 0 ? s.hg : 1, s.tok) ||
+      !make_thd_map(&tdo, dsrc, s.d, hq_map, rq, s.total_q > 0 ? s.hg : 1, s.tok) ||
+      !make_thd_map(&tk, k, s.d, s.hkv, s.total_k, 1, kTileN) ||
+      !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN))
+    return tensor_map_error();
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  BwdArgs a{};
+  a.items = reinterpret_cast<const BwdItem*>(w + kHeaderBytes + sizeof(FwdItem) * size_t(s.n_fwd));
+  a.lse = lse;
+  a.D = reinterpret_cast<const float*>(w + ws_offset_D(s));
+  a.dq_acc = reinterpret_cast<float*>(w + ws_offset_dqacc(s));
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.timeout_ns = kTimeoutNs;
+  a.hq = s.hq;
+  a.hkv = s.hkv;
+  a.G = s.G;
+  a.hg = s.hg;
+  a.lg_hg = s.lg_hg;
+  a.tok = s.tok;
+  a.total_q = int(s.total_q);
+  a.block = s.B;
+  a.scale = s.scale;
+  a.scale_log2 = s.scale * 1.4426950408889634f;
+  return cuda_status(launch_bwd_dkdv(s.d, tq, tk, tv, tdo, a, s.n_bwd,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bda_status bda_attn_bwd_dq_convert(const bda_problem* prob, const bda_mask_desc* mask, void* dq,
+                                   void* ws, size_t ws_bytes, bda_stream_t stream) {
+  Shape s;
+  bda_status st = validate(prob, mask, &s);
+  if (st != BDA_OK) return st;
+  if ((st = check_ws(s, ws, ws_bytes, true)) != BDA_OK) return st;
+  if (s.total_q == 0) return BDA_OK;
+  if (!dq || !aligned16(dq)) return BDA_ERR_INVALID_ARG;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  return cuda_status(launch_dq_convert(s.d, reinterpret_cast<const float*>(w + ws_offset_dqacc(s)),
+                                       static_cast<__nv_bfloat16*>(dq), s.total_q, s.hq, s.scale,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bda_status bda_attn_bwd(const bda_problem* prob, const bda_mask_desc* mask, const void* q,
+                        const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                        bda_stream_t stream) {
+  // Every argument of all three stages is checked before the first launch.
+  Shape s;
+  bda_status st = validate(prob, mask, &s);
+  if (st != BDA_OK) return st;
+  if ((st = check_ws(s, ws, ws_bytes, true)) != BDA_OK) return st;
+  const void* need_q[] = {q, o, lse, dout, dq};
+  const void* need_k[] = {k, v, dk, dv};
+  for (const void* p : need_q)
+    if ((s.total_q > 0 && !p) || !aligned16(p)) return BDA_ERR_INVALID_ARG;
+  for (const void* p : need_k)
+    if ((s.total_k > 0 && !p) || !aligned16(p)) return BDA_ERR_INVALID_ARG;
+  st = bda_attn_bwd_preprocess(prob, mask, o, dout, ws, ws_bytes, stream);
+  if (st != BDA_OK) return st;
+  st = bda_attn_bwd_dkdv(prob, mask, q, k, v, lse, dout, dk, dv, ws, ws_bytes, stream);
+  if (st != BDA_OK) return st;
+  return bda_attn_bwd_dq_convert(prob, mask, dq, ws, ws_bytes, stream);
+}
+
+bda_status bda_attn_check_status(void* ws, size_t ws_bytes, bda_stream_t stream) {
+  if (!ws || ws_bytes < sizeof(uint32_t)) return BDA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  bda_status r;
+  if ((r = cuda_status(cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, st))) != BDA_OK)
+    return r;
+  if ((r = cuda_status(cudaStreamSynchronize(st))) != BDA_OK) return r;
+  if (v == 0) return BDA_OK;
+  if ((r = cuda_status(cudaMemsetAsync(ws, 0, sizeof(uint32_t), st))) != BDA_OK) return r;
+  if ((r = cuda_status(cudaStreamSynchronize(st))) != BDA_OK) return r;
+  return BDA_ERR_DEVICE_TIMEOUT;
+}
+
+const char* bda_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* bda_status_string(bda_status s) {
+  switch (s) {
+    case BDA_OK: return "ok";
+    case BDA_ERR_INVALID_ARG: return "invalid argument";
+    case BDA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case BDA_ERR_WORKSPACE: return "workspace or plan buffer too small";
+    case BDA_ERR_CUDA: return "CUDA error";
+    case BDA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,524 @@
+// bda_bwd.cu -- backward block-causal / staircase attention for sm_103a.
+//
+// The staircase kernel of the ORL announcement thread (24vids.com mirror),
+// Insight 3, serves training ("up to 5.2x faster training"), so it needs the
+// gradients.  Textbook softmax-attention backward with the forward's LSE:
+//   P = exp(scale S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO o O),
+//   dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+// Three stages:
+//   1. bwd_preprocess: D (fp32 [hq][total_q]) and a zeroed fp32 dQ accumulator.
+//   2. bwd_dkdv: one CTA per (128-key tile, KV head).  dK and dV accumulate in
+//      TMEM over every query tile (tok tokens x hg heads of the group) that
+//      sees the key tile; the mask comes from block indices.  Per query tile:
+//        S^T  = K Q^T            (tcgen05, TMEM)
+//        P^T  -> bf16 smem       (softmax warps, thread = key row)
+//        dP^T = V dO^T           (tcgen05, TMEM)
+//        dV  += P^T dO           (tcgen05, A from smem)
+//        dS^T -> bf16 smem       (softmax warps)
+//        dK  += dS^T Q           (tcgen05)
+//        dQ_t = dS K             (tcgen05, A = the same dS^T buffer read MN-major)
+//      and the dQ partial is added to the fp32 accumulator with vector
+//      reductions by a second warpgroup.
+//   3. dq_convert: dQ = bf16(scale * accumulator).
+// Roles of the dK/dV kernel (320 threads):
+//   warps 0..3   softmax: P^T and dS^T, then the dK epilogue
+//   warps 4..7   dQ readout + global reductions, then the dV epilogue
+//   warp 8       producer: K/V once, then Q, dO (TMA) and LSE, D per query tile
+//   warp 9       MMA issuer (one thread)
+// TMEM columns: S^T [0,128) dP^T / dQ [128,256) dK [256,256+D) dV [384,384+D).
+#include <cuda_bf16.h>
+
+#include "bda_internal.h"
+#include "bda_kernels.h"
+#include "bda_ptx.cuh"
+
+namespace bda {
+
+namespace {
+
+// ------------------------------------------------------------- preprocess
+template <int D>
+__global__ void __launch_bounds__(256) bda_bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                                                                 const __nv_bfloat16* __restrict__ dout,
+                                                                 float* __restrict__ Dv,
+                                                                 float* __restrict__ dq_acc,
+                                                                 int64_t total_q, int hq) {
+  constexpr int PER = D / 32;  // elements per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = total_q * hq;
+  const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = warp0; row < rows; row += nwarps) {
+    const __nv_bfloat16* po = o + row * D + lane * PER;
+    const __nv_bfloat16* pd = dout + row * D + lane * PER;
+    float acc = 0.f;
+    if constexpr (PER == 4) {
+      const uint2 a = *reinterpret_cast<const uint2*>(po);
+      const uint2 b = *reinterpret_cast<const uint2*>(pd);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float2 x = __bfloat1622float2(a2[j]), y = __bfloat1622float2(b2[j]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+      *reinterpret_cast<float4*>(dq_acc + row * D + lane * PER) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(po);
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(pd);
+      const float2 x = __bfloat1622float2(a), y = __bfloat1622float2(b);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+      *reinterpret_cast<float2*>(dq_acc + row * D + lane * PER) = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      const int64_t t = row / hq, h = row - t * hq;
+      Dv[h * total_q + t] = acc;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- convert
+__global__ void __launch_bounds__(256) bda_dq_convert_kernel(const float* __restrict__ acc,
+                                                             __nv_bfloat16* __restrict__ dq,
+                                                             int64_t n8, float scale) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    uint4 out;
+    out.x = pack_bf16x2(a.x * scale, a.y * scale);
+    out.y = pack_bf16x2(a.z * scale, a.w * scale);
+    out.z = pack_bf16x2(b.x * scale, b.y * scale);
+    out.w = pack_bf16x2(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = out;
+  }
+}
+
+// ------------------------------------------------------------------ dK/dV
+constexpr int kBwdThreads = 320;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
+
+template <int D>
+struct BwdLayout {
+  static constexpr int CH = D / 64;
+  static constexpr uint32_t CHUNK = 128 * 128;  // [128 rows][64 bf16], 128B-swizzled
+  static constexpr uint32_t TILE = CH * CHUNK;  // a K, V, Q or dO tile
+  static constexpr uint32_t PT = 2 * CHUNK;     // [128 keys][128 query cols] bf16
+  static constexpr uint32_t K = 0;
+  static constexpr uint32_t V = K + TILE;
+  static constexpr uint32_t Q = V + TILE;
+  static constexpr uint32_t DO = Q + TILE;
+  static constexpr uint32_t P = DO + TILE;
+  static constexpr uint32_t DS = P + PT;
+  static constexpr uint32_t LSE = DS + PT;      // float[128]: LSE * log2(e) per query col
+  static constexpr uint32_t DD = LSE + 512;     // float[128]: D per query col
+  static constexpr uint32_t BAR = DD + 512;
+  static constexpr int B_KV = 0, B_QFULL = 1, B_SFULL = 2, B_SFREE = 3, B_DPFULL = 4,
+                       B_DQFREE = 5, B_PFULL = 6, B_DSFULL = 7, B_DQFULL = 8, B_QEMPTY = 9,
+                       B_ACC = 10, NBAR = 11;
+  static constexpr uint32_t MISC = BAR + 8 * NBAR;
+  static constexpr uint32_t BYTES = MISC + 16;
+  static constexpr uint32_t ALLOC = BYTES + 1024;
+};
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ bool drain_wait(WaitCtx w, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > w.timeout_ns) {
+      atomicOr(w.status, kDeviceTimeoutCode);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                        const BwdArgs a) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto bar = [&](int i) -> uint32_t { return base + L::BAR + 8u * uint32_t(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::MISC + 4);
+  float* s_lse = reinterpret_cast<float*>(gbase + L::LSE);
+  float* s_D = reinterpret_cast<float*>(gbase + L::DD);
+
+  const int item_idx = blockIdx.x / a.hkv;
+  const int kvh = blockIdx.x - item_idx * a.hkv;
+  const BwdItem it = a.items[item_idx];
+  const int n_sub = a.G / a.hg;
+  const int n_iter = it.work;  // query tiles: token tiles x head sub-groups
+  const int delta = it.lk - it.lq;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(L::B_KV), 1);
+    mbar_init(bar(L::B_QFULL), 32);
+    mbar_init(bar(L::B_SFULL), 1);
+    mbar_init(bar(L::B_SFREE), 128);
+    mbar_init(bar(L::B_DPFULL), 1);
+    mbar_init(bar(L::B_DQFREE), 128);
+    mbar_init(bar(L::B_PFULL), 128);
+    mbar_init(bar(L::B_DSFULL), 128);
+    mbar_init(bar(L::B_DQFULL), 1);
+    mbar_init(bar(L::B_QEMPTY), 1);
+    mbar_init(bar(L::B_ACC), 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const WaitCtx wc{abort_flag, a.status, a.timeout_ns};
+  // query tile i: token tile t0 (local) and head sub-group sub
+  auto tile_t0 = [&](int i) -> int { return it.q_begin + (i / n_sub) * a.tok; };
+  auto tile_h0 = [&](int i) -> int { return kvh * a.G + (i % n_sub) * a.hg; };
+
+  bool ok = true;
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    if (n_iter > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+        mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::TILE);
+        for (int c = 0; c < L::CH; ++c) {
+          tma_load_3d(base + L::K + c * L::CHUNK, &tm_k, bar(L::B_KV), c * 64, kvh, it.k_row);
+          tma_load_3d(base + L::V + c * L::CHUNK, &tm_v, bar(L::B_KV), c * 64, kvh, it.k_row);
+        }
+      }
+      for (int i = 0; i < n_iter; ++i) {
+        if (i > 0 && !mbar_wait_warp(wc, bar(L::B_QEMPTY), uint32_t(i - 1) & 1u)) { ok = false; break; }
+        const int t0 = tile_t0(i), h0 = tile_h0(i);
+        if (lane == 0) {
+          expect_tx(bar(L::B_QFULL), 2 * L::TILE);
+          for (int c = 0; c < L::CH; ++c) {
+            tma_load_3d(base + L::Q + c * L::CHUNK, &tm_q, bar(L::B_QFULL), c * 64, h0, it.q_row + t0);
+            tma_load_3d(base + L::DO + c * L::CHUNK, &tm_do, bar(L::B_QFULL), c * 64, h0,
+                        it.q_row + t0);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int col = lane + 32 * k;
+          const int tok = t0 + (col >> a.lg_hg);
+          const int h = h0 + (col & (a.hg - 1));
+          float lv = INFINITY, dv = 0.f;
+          if (tok < it.lq) {
+            const size_t idx = size_t(h) * size_t(a.total_q) + size_t(it.q_row + tok);
+            lv = a.lse[idx] * 1.4426950408889634f;
+            dv = a.D[idx];
+          }
+          s_lse[col] = lv;
+          s_D[col] = dv;
+        }
+        mbar_arrive(bar(L::B_QFULL));
+        ++issued;
+      }
+      if (!ok || *abort_flag) {
+        if (lane == 0) {
+          drain_wait(wc, bar(L::B_KV), 0);
+          if (issued) drain_wait(wc, bar(L::B_QFULL), uint32_t(issued - 1) & 1u);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0 && n_iter > 0) {
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
+      constexpr uint32_t idAcc = idesc_bf16(128, D, false, true);     // dV, dK
+      constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);       // dQ
+      ok = mbar_wait(wc, bar(L::B_KV), 0);
+      for (int i = 0; ok && i < n_iter; ++i) {
+        const uint32_t ph = uint32_t(i) & 1u, php = uint32_t(i - 1) & 1u;
+        if (!mbar_wait(wc, bar(L::B_QFULL), ph)) { ok = false; break; }
+        if (i > 0 && !mbar_wait(wc, bar(L::B_SFREE), php)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+          mma_ss(tbase + kColS, sdesc_sw128(base + L::K + off, 16, 1024),
+                 sdesc_sw128(base + L::Q + off, 16, 1024), idSS, kk > 0);
+        }
+        mma_commit(bar(L::B_SFULL));
+        if (i > 0 && !mbar_wait(wc, bar(L::B_DQFREE), php)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+          mma_ss(tbase + kColDP, sdesc_sw128(base + L::V + off, 16, 1024),
+                 sdesc_sw128(base + L::DO + off, 16, 1024), idSS, kk > 0);
+        }
+        mma_commit(bar(L::B_DPFULL));
+        if (!mbar_wait(wc, bar(L::B_PFULL), ph)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTileM / 16; ++kk) {
+          const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+          mma_ss(tbase + kColDV, sdesc_sw128(base + L::P + aoff, 16, 1024),
+                 sdesc_sw128(base + L::DO + 2048u * kk, L::CHUNK, 1024), idAcc,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!mbar_wait(wc, bar(L::B_DSFULL), ph)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTileM / 16; ++kk) {
+          const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+          mma_ss(tbase + kColDK, sdesc_sw128(base + L::DS + aoff, 16, 1024),
+                 sdesc_sw128(base + L::Q + 2048u * kk, L::CHUNK, 1024), idAcc,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ss(tbase + kColDP, sdesc_sw128(base + L::DS + 2048u * kk, L::CHUNK, 1024),
+                 sdesc_sw128(base + L::K + 2048u * kk, L::CHUNK, 1024), idDQ, kk > 0);
+        mma_commit(bar(L::B_DQFULL));
+        mma_commit(bar(L::B_QEMPTY));
+      }
+      mma_commit(bar(L::B_ACC));
+      drain_wait(wc, bar(L::B_ACC), 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------- softmax
+    const int kr = tid;  // TMEM lane == key row of the tile
+    const bool key_valid = kr < it.k_len;
+    const KeyRows kq = key_rows(it.kpos0 + kr, it.prefix, a.block, it.lk);
+    const int q_hi = min(kq.hi - delta, it.lq);  // local query tokens [kq.lo - delta, q_hi)
+    const uint32_t lane_addr = tbase + (uint32_t(warp * 32) << 16);
+    const float sl2 = a.scale_log2;
+    for (int i = 0; i < n_iter; ++i) {
+      const uint32_t ph = uint32_t(i) & 1u;
+      const int t0 = tile_t0(i);
+      const int lo_c = key_valid ? kq.lo - delta - t0 : 0;
+      const int hi_c = key_valid ? q_hi - t0 : 0;
+      const unsigned span = hi_c > lo_c ? unsigned(hi_c - lo_c) : 0u;
+      const bool full = lo_c <= 0 && hi_c >= a.tok;
+      // QFULL publishes the producer's LSE / D staging to these threads.
+      if (!mbar_wait_warp(wc, bar(L::B_QFULL), ph)) { ok = false; break; }
+      if (!mbar_wait_warp(wc, bar(L::B_SFULL), ph)) { ok = false; break; }
+      tc_fence_after();
+      // P^T = exp(scale S^T - LSE), masked, 32 columns at a time; kept packed
+      // (bf16 pairs, the values the dV MMA sees) for dS, and stored into smem
+      // as the K-major A operand of dV += P^T dO.
+      uint32_t pp[kTileM / 2];
+      uint8_t* sp = gbase + L::P;
+#pragma unroll
+      for (int c = 0; c < kTileM / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + kColS + 32u * c, rr);
+        tmem_ld_wait(rr);
+        if (c == kTileM / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(L::B_SFREE));
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c0 = 32 * c + 2 * j, c1 = c0 + 1;
+          float p0 = ex2(fmaf(__uint_as_float(rr[2 * j]), sl2, -s_lse[c0]));
+          float p1 = ex2(fmaf(__uint_as_float(rr[2 * j + 1]), sl2, -s_lse[c1]));
+          if (!full) {
+            if (unsigned((c0 >> a.lg_hg) - lo_c) >= span) p0 = 0.f;
+            if (unsigned((c1 >> a.lg_hg) - lo_c) >= span) p1 = 0.f;
+          }
+          pp[16 * c + j] = pack_bf16x2(p0, p1);
+        }
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          const int u = 4 * c + u4;
+          *reinterpret_cast<uint4*>(sp + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =
+              make_uint4(pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::B_PFULL));
+      // dS^T = P^T o (dP^T - D)
+      if (!mbar_wait_warp(wc, bar(L::B_DPFULL), ph)) { ok = false; break; }
+      tc_fence_after();
+      uint8_t* sds = gbase + L::DS;
+#pragma unroll
+      for (int c = 0; c < kTileM / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + kColDP + 32u * c, rr);
+        tmem_ld_wait(rr);
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int cc = 8 * u4 + 2 * j;
+            const int c0 = 32 * c + cc;
+            const uint32_t pb = pp[c0 >> 1];
+            const float d0 = __uint_as_float(pb << 16) * (__uint_as_float(rr[cc]) - s_D[c0]);
+            const float d1 = __uint_as_float(pb & 0xffff0000u) *
+                             (__uint_as_float(rr[cc + 1]) - s_D[c0 + 1]);
+            pk[j] = pack_bf16x2(d0, d1);
+          }
+          const int u = 4 * c + u4;
+          *reinterpret_cast<uint4*>(sds + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::B_DSFULL));
+    }
+  } else {
+    // ------------------------------------------------------ dQ reductions
+    const int qc = tid - 128;  // TMEM lane == query column of the tile
+    const uint32_t lane_addr = tbase + (uint32_t((warp - 4) * 32) << 16);
+    for (int i = 0; i < n_iter; ++i) {
+      if (!mbar_wait_warp(wc, bar(L::B_DQFULL), uint32_t(i) & 1u)) { ok = false; break; }
+      tc_fence_after();
+      float dq[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + kColDP + 32u * c, rr);
+        tmem_ld_wait(rr);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dq[32 * c + j] = __uint_as_float(rr[j]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::B_DQFREE));
+      const int tok = tile_t0(i) + (qc >> a.lg_hg);
+      if (tok < it.lq) {
+        const int h = tile_h0(i) + (qc & (a.hg - 1));
+        float* dst = a.dq_acc + (size_t(it.q_row + tok) * size_t(a.hq) + size_t(h)) * size_t(D);
+#pragma unroll
+        for (int j = 0; j < D; j += 4) red_add_v4(dst + j, dq[j], dq[j + 1], dq[j + 2], dq[j + 3]);
+      }
+    }
+  }
+
+  // ----------------------------------------------- dK (warps 0-3), dV (4-7)
+  if (warp < 8) {
+    const int row = tid & 127;
+    const bool is_dk = warp < 4;
+    const uint32_t lane_addr = tbase + (uint32_t((warp & 3) * 32) << 16);
+    const bool have = n_iter > 0 && ok && !*abort_flag;
+    bool acc_ok = false;
+    if (have) acc_ok = mbar_wait_warp(wc, bar(L::B_ACC), 0);
+    if (have && acc_ok) tc_fence_after();
+    if (n_iter == 0 || acc_ok) {
+      __nv_bfloat16* dst = (is_dk ? a.dk : a.dv) +
+                           (size_t(it.k_row + row) * size_t(a.hkv) + size_t(kvh)) * size_t(D);
+      const float mul = is_dk ? a.scale : 1.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        if (n_iter > 0) {
+          tmem_ld32(lane_addr + (is_dk ? kColDK : kColDV) + 32u * c, rr);
+          tmem_ld_wait(rr);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rr[j] = 0u;
+        }
+        if (row < it.k_len) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(__uint_as_float(rr[2 * j]) * mul, __uint_as_float(rr[2 * j + 1]) * mul);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdArgs& a, int n_items, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  cudaError_t e = cudaFuncSetAttribute(bda_bwd_dkdv_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::ALLOC));
+  if (e != cudaSuccess) return e;
+  const unsigned grid = unsigned(n_items) * unsigned(a.hkv);
+  bda_bwd_dkdv_kernel<D><<<grid, kBwdThreads, L::ALLOC, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+int sm_count() {
+  static int n = [] {
+    int dev = 0, v = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      return v;
+    return 148;
+  }();
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(int head_dim, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                                  float* D, float* dq_acc, int64_t total_q, int hq,
+                                  cudaStream_t stream) {
+  const int64_t rows = total_q * hq;
+  if (rows == 0) return cudaSuccess;
+  int64_t blocks = (rows + 7) / 8;  // 8 warps per block, one row per warp per pass
+  const int64_t cap = int64_t(sm_count()) * 16;
+  if (blocks > cap) blocks = cap;
+  if (head_dim == 128)
+    bda_bwd_preprocess_kernel<128><<<unsigned(blocks), 256, 0, stream>>>(o, dout, D, dq_acc, total_q, hq);
+  else
+    bda_bwd_preprocess_kernel<64><<<unsigned(blocks), 256, 0, stream>>>(o, dout, D, dq_acc, total_q, hq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                            int n_items, cudaStream_t stream) {
+  if (n_items == 0) return cudaSuccess;
+  if (head_dim == 128) return launch_dkdv_t<128>(tq, tk, tv, tdo, a, n_items, stream);
+  return launch_dkdv_t<64>(tq, tk, tv, tdo, a, n_items, stream);
+}
+
+cudaError_t launch_dq_convert(int head_dim, const float* dq_acc, __nv_bfloat16* dq, int64_t total_q,
+                              int hq, float scale, cudaStream_t stream) {
+  const int64_t n8 = total_q * hq * head_dim / 8;
+  if (n8 == 0) return cudaSuccess;
+  int64_t blocks = (n8 + 255) / 256;
+  const int64_t cap = int64_t(sm_count()) * 16;
+  if (blocks > cap) blocks = cap;
+  bda_dq_convert_kernel<<<unsigned(blocks), 256, 0, stream>>>(dq_acc, dq, n8, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace bda

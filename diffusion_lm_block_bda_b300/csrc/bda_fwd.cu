@@ -1,0 +1,343 @@
+// bda_fwd.cu -- forward block-causal / staircase attention for sm_103a.
+//
+// The forward of the attention the ORL announcement thread (24vids.com
+// mirror), highlight 3, says was redesigned for block-causal masks, and the
+// staircase replay of Insight 3 / the ORL paper card's Figure 3 caption.
+// FlashAttention-style: per 128-row query tile the key tiles stream through
+// shared memory and an online softmax keeps a running max and sum, so the
+// L x L score matrix never exists.
+//
+// One CTA per (query tile, group of hg query heads); the tile is tok = 128/hg
+// tokens x hg heads of one KV group, so the KV heads' K/V tile feeds all 128
+// rows (GQA packing).  Roles:
+//   warp 4        TMA producer: Q once, then K and V tiles (NST-stage ring)
+//   warp 5        tcgen05 MMA issuer (one thread): S = Q K^T into TMEM
+//                 (double buffered), O += P V with P read from TMEM
+//   warps 0..3    softmax: thread r owns TMEM lane r = query row r; masks
+//                 PARTIAL tiles from block indices, online max/sum, writes P
+//                 as bf16 into TMEM, rescales O when the max grows by more
+//                 than 2^8, and runs the epilogue (O / l, LSE).
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+D) P [384,448).
+#include <cuda_bf16.h>
+
+#include "bda_internal.h"
+#include "bda_kernels.h"
+#include "bda_ptx.cuh"
+
+namespace bda {
+
+namespace {
+
+constexpr int kFwdThreads = 192;
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
+
+template <int D, int NST>
+struct FwdLayout {
+  static constexpr int CH = D / 64;              // 128-byte chunks of a head_dim row
+  static constexpr uint32_t CHUNK = 128 * 128;   // one [128 rows][64 bf16] swizzled chunk
+  static constexpr uint32_t TILE = CH * CHUNK;
+  static constexpr uint32_t Q = 0;
+  static constexpr uint32_t K = Q + TILE;
+  static constexpr uint32_t V = K + NST * TILE;
+  static constexpr uint32_t BAR = V + NST * TILE;
+  // q_full, k_full[NST], k_empty[NST], v_full[NST], v_empty[NST],
+  // s_full[2], s_free[2], p_full, o_done, drain
+  static constexpr int B_QFULL = 0;
+  static constexpr int B_KFULL = 1;
+  static constexpr int B_KEMPTY = B_KFULL + NST;
+  static constexpr int B_VFULL = B_KEMPTY + NST;
+  static constexpr int B_VEMPTY = B_VFULL + NST;
+  static constexpr int B_SFULL = B_VEMPTY + NST;
+  static constexpr int B_SFREE = B_SFULL + 2;
+  static constexpr int B_PFULL = B_SFREE + 2;
+  static constexpr int B_ODONE = B_PFULL + 1;
+  static constexpr int B_DRAIN = B_ODONE + 1;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr uint32_t MISC = BAR + 8 * NBAR;
+  static constexpr uint32_t BYTES = MISC + 16;
+  static constexpr uint32_t ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
+};
+
+// Bounded wait that ignores the abort flag: used to let in-flight copies and
+// MMAs land before a CTA leaves (normal path and abort path alike).
+__device__ __forceinline__ bool drain_wait(WaitCtx w, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > w.timeout_ns) {
+      atomicOr(w.status, kDeviceTimeoutCode);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int D, int NST>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    bda_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using L = FwdLayout<D, NST>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto bar = [&](int i) -> uint32_t { return base + L::BAR + 8u * uint32_t(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::MISC + 4);
+
+  const int item_idx = blockIdx.x / a.n_groups;
+  const int grp = blockIdx.x - item_idx * a.n_groups;
+  const FwdItem it = a.items[item_idx];
+  const int head0 = grp * a.hg;
+  const int kvh = head0 / a.G;
+  const int n_tiles = it.r1_end + (it.r2_end - it.r2_begin);
+  auto key_tile = [&](int n) -> int { return n < it.r1_end ? n : it.r2_begin + (n - it.r1_end); };
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(L::B_QFULL), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar(L::B_KFULL + s), 1);
+      mbar_init(bar(L::B_KEMPTY + s), 1);
+      mbar_init(bar(L::B_VFULL + s), 1);
+      mbar_init(bar(L::B_VEMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::B_SFULL + b), 1);
+      mbar_init(bar(L::B_SFREE + b), 128);
+    }
+    mbar_init(bar(L::B_PFULL), 128);
+    mbar_init(bar(L::B_ODONE), 1);
+    mbar_init(bar(L::B_DRAIN), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const WaitCtx wc{abort_flag, a.status, a.timeout_ns};
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int nk[NST], nv[NST];
+      for (int s = 0; s < NST; ++s) nk[s] = nv[s] = 0;
+      mbar_arrive_expect_tx(bar(L::B_QFULL), L::TILE);
+      for (int c = 0; c < L::CH; ++c)
+        tma_load_3d(base + L::Q + c * L::CHUNK, &tm_q, bar(L::B_QFULL), c * 64, head0, it.q_row);
+      bool ok = true;
+      for (int n = 0; n < n_tiles && ok; ++n) {
+        const int s = n % NST;
+        const uint32_t ph = uint32_t(n / NST) & 1u;
+        const int krow = it.k_row + key_tile(n) * kTileN;
+        if (n >= NST && !mbar_wait(wc, bar(L::B_KEMPTY + s), ph ^ 1u)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(L::B_KFULL + s), L::TILE);
+        for (int c = 0; c < L::CH; ++c)
+          tma_load_3d(base + L::K + s * L::TILE + c * L::CHUNK, &tm_k, bar(L::B_KFULL + s), c * 64,
+                      kvh, krow);
+        ++nk[s];
+        if (n >= NST && !mbar_wait(wc, bar(L::B_VEMPTY + s), ph ^ 1u)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::TILE);
+        for (int c = 0; c < L::CH; ++c)
+          tma_load_3d(base + L::V + s * L::TILE + c * L::CHUNK, &tm_v, bar(L::B_VFULL + s), c * 64,
+                      kvh, krow);
+        ++nv[s];
+      }
+      if (!ok || *abort_flag) {
+        // Let every copy already issued land before the CTA can exit.
+        drain_wait(wc, bar(L::B_QFULL), 0);
+        for (int s = 0; s < NST; ++s) {
+          if (nk[s]) drain_wait(wc, bar(L::B_KFULL + s), uint32_t(nk[s] - 1) & 1u);
+          if (nv[s]) drain_wait(wc, bar(L::B_VFULL + s), uint32_t(nv[s] - 1) & 1u);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      bool ok = mbar_wait(wc, bar(L::B_QFULL), 0);
+      auto issue_s = [&](int n) -> bool {
+        const int s = n % NST, b = n & 1;
+        if (!mbar_wait(wc, bar(L::B_KFULL + s), uint32_t(n / NST) & 1u)) return false;
+        if (n >= 2 && !mbar_wait(wc, bar(L::B_SFREE + b), uint32_t((n >> 1) - 1) & 1u)) return false;
+        tc_fence_after();
+        const uint32_t qa = base + L::Q, ka = base + L::K + s * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+          mma_ss(tbase + kColS + 128u * b, sdesc_sw128(qa + off, 16, 1024),
+                 sdesc_sw128(ka + off, 16, 1024), idS, kk > 0);
+        }
+        mma_commit(bar(L::B_SFULL + b));
+        mma_commit(bar(L::B_KEMPTY + s));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int n = 0; ok && n < n_tiles; ++n) {
+        if (n + 1 < n_tiles && !issue_s(n + 1)) { ok = false; break; }
+        const int s = n % NST;
+        if (!mbar_wait(wc, bar(L::B_PFULL), uint32_t(n) & 1u)) { ok = false; break; }
+        if (!mbar_wait(wc, bar(L::B_VFULL + s), uint32_t(n / NST) & 1u)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t va = base + L::V + s * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ts(tbase + kColO, tbase + kColP + 8u * kk, sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024),
+                 idO, (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::B_ODONE));
+        mma_commit(bar(L::B_VEMPTY + s));
+      }
+      // Every MMA issued above completes before TMEM can be released.
+      mma_commit(bar(L::B_DRAIN));
+      drain_wait(wc, bar(L::B_DRAIN), 0);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int r = tid;  // TMEM lane == query row of the tile
+    const int t_local = r >> a.lg_hg;
+    const int hh = r & (a.hg - 1);
+    const bool row_valid = t_local < it.q_len;
+    const int p = it.pos0 + (row_valid ? t_local : it.q_len - 1);
+    const RowKeys rk = row_keys(p, it.prefix, a.block, it.lk);
+    const uint32_t lane_addr = tbase + (uint32_t(warp * 32) << 16);
+    const float sl2 = a.scale_log2;
+    float m_ref = -INFINITY;  // running max of scale*log2(e)*S, the reference of P
+    float l = 0.f;            // running sum of P (relative to m_ref)
+    bool ok = true;
+    for (int n = 0; n < n_tiles; ++n) {
+      const int b = n & 1;
+      if (!mbar_wait_warp(wc, bar(L::B_SFULL + b), uint32_t(n >> 1) & 1u)) { ok = false; break; }
+      tc_fence_after();
+      float sv[kTileN];
+#pragma unroll
+      for (int c = 0; c < kTileN / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + kColS + 128u * b + 32u * c, rr);
+        tmem_ld_wait(rr);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[32 * c + j] = __uint_as_float(rr[j]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::B_SFREE + b));
+      if (n >= it.n_full) {  // PARTIAL tile: mask from block indices
+        const int k0 = key_tile(n) * kTileN;
+        const int ca = rk.a - k0, cb = rk.b - k0, ce = rk.e - k0;
+#pragma unroll
+        for (int j = 0; j < kTileN; ++j)
+          if (!(j < ca || (j >= cb && j < ce))) sv[j] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int j = 1; j < kTileN; ++j) mx = fmaxf(mx, sv[j]);
+      const float m_cand = mx * sl2;
+      float alpha = 1.f;
+      if (m_cand > m_ref + kRescaleThreshold) {
+        alpha = ex2(m_ref - m_cand);  // 0 on the first finite max
+        m_ref = m_cand;
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // P of the previous tile is still read by its PV MMA, and O must be
+      // complete before a rescale: wait for PV(n-1).
+      if (n > 0) {
+        if (!mbar_wait_warp(wc, bar(L::B_ODONE), uint32_t(n - 1) & 1u)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(lane_addr + kColO + 32u * c, rr);
+            tmem_ld_wait(rr);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+            tmem_st32(lane_addr + kColO + 32u * c, rr);
+          }
+        }
+      }
+      float rowsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kTileN / 64; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float p0 = ex2(fmaf(sv[64 * c + 2 * j], sl2, -m_use));
+          const float p1 = ex2(fmaf(sv[64 * c + 2 * j + 1], sl2, -m_use));
+          rowsum += p0 + p1;
+          pk[j] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(lane_addr + kColP + 32u * c, pk);
+      }
+      l = l * alpha + rowsum;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::B_PFULL));
+    }
+    if (ok && mbar_wait_warp(wc, bar(L::B_ODONE), uint32_t(n_tiles - 1) & 1u)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow =
+          a.o + (size_t(it.q_row + t_local) * a.hq + size_t(head0 + hh)) * size_t(D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + kColO + 32u * c, rr);
+        tmem_ld_wait(rr);
+        if (row_valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(__uint_as_float(rr[2 * j]) * inv_l,
+                                __uint_as_float(rr[2 * j + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      if (row_valid) {
+        const float lse2 = m_ref + log2f(l);
+        a.lse[size_t(head0 + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
+            lse2 * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, int NST>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdArgs& a, int n_items, cudaStream_t stream) {
+  using L = FwdLayout<D, NST>;
+  cudaError_t e = cudaFuncSetAttribute(bda_fwd_kernel<D, NST>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::ALLOC));
+  if (e != cudaSuccess) return e;
+  const unsigned grid = unsigned(n_items) * unsigned(a.n_groups);
+  bda_fwd_kernel<D, NST><<<grid, kFwdThreads, L::ALLOC, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdArgs& a, int n_items, cudaStream_t stream) {
+  if (n_items == 0) return cudaSuccess;
+  if (head_dim == 128) return launch_fwd_t<128, 2>(tq, tk, tv, a, n_items, stream);
+  return launch_fwd_t<64, 2>(tq, tk, tv, a, n_items, stream);
+}
+
+}  // namespace bda

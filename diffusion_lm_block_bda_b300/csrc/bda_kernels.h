@@ -1,0 +1,59 @@
+// bda_kernels.h -- launchers of the CUDA kernels (internal; the public surface
+// is include/bda_attn.h).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "bda_internal.h"
+
+namespace bda {
+
+struct FwdArgs {
+  const FwdItem* items;
+  __nv_bfloat16* o;
+  float* lse;
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int n_groups;  // hq / hg: CTAs per work item
+  int hg, lg_hg;
+  int G;         // hq / hkv
+  int hq;
+  int total_q;
+  int block;
+  float scale_log2;  // softmax_scale * log2(e)
+};
+
+struct BwdArgs {
+  const BwdItem* items;
+  const float* lse;      // [hq][total_q]
+  const float* D;        // [hq][total_q]
+  float* dq_acc;         // [total_q][hq][d], unscaled sum of dS K
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int hq, hkv, G;
+  int hg, lg_hg, tok;
+  int total_q;
+  int block;
+  float scale;       // softmax_scale
+  float scale_log2;  // softmax_scale * log2(e)
+};
+
+cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdArgs& a, int n_items, cudaStream_t stream);
+
+cudaError_t launch_bwd_preprocess(int head_dim, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                                  float* D, float* dq_acc, int64_t total_q, int hq,
+                                  cudaStream_t stream);
+
+cudaError_t launch_bwd_dkdv(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                            int n_items, cudaStream_t stream);
+
+cudaError_t launch_dq_convert(int head_dim, const float* dq_acc, __nv_bfloat16* dq, int64_t total_q,
+                              int hq, float scale, cudaStream_t stream);
+
+}  // namespace bda

