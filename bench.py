@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark: useful TFLOPS of forward + backward block-causal attention on the
+packed training-replay workload (16 packed sequences, lengths U[512, 4096]
+rounded to 32, block 32, 32 query / 8 KV heads, head_dim 128, bf16).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+One step is one pass of the whole hot path over one batch: the tile plan
+(host, copied to the workspace), the forward kernel and the three backward
+stages, on inputs already resident in HBM.  `value` counts useful FLOPs only
+(4 d Hq pairs forward + 10 d Hq pairs backward, pairs = allowed (query, key)
+pairs).  `e2e` repeats the step through the same public API with the inputs
+copied from pinned host memory and every output (O, LSE, dQ, dK, dV) copied
+back inside the timed region.  With N > 1 (torchrun, one rank per GPU) the
+global batch holds 16 N sequences, sharded whole by longest-first load
+balancing with no collective on the data path (weak scaling); the timing is
+the max over ranks.
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload, on the host cores.
+"""
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from diffusion_lm_block_bda_b300 import workloads as W  # noqa: E402
+
+METRIC = "useful TFLOPS and % of B300 BF16 peak, fwd+bwd block-causal/staircase attention"
+UNIT = "TFLOPS"
+WORKLOAD_NAME = "packed block-causal training replay: 16 seqs U[512,4096]/32*32, B=32, Hq=32, Hkv=8, d=128"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------ distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- workload
+def rank_workload(world, rank):
+    """Global batch of 16 * world packed sequences (seed 0), LPT-sharded."""
+    from diffusion_lm_block_bda_b300 import sharding
+    gen = torch.Generator().manual_seed(0)
+    lens = W.packed_lengths(gen, n=16 * world)
+    full = W.Workload("packed_block_causal_16xU512_4096_B32", W.BLOCK_CAUSAL, 32, 32, 8, 128,
+                      lens, list(lens))
+    if world == 1:
+        return full, list(range(len(lens)))
+    shards = sharding.lpt_shard(sharding.sequence_costs(full), world)
+    return sharding.subset(full, shards[rank], f"_rank{rank}"), shards[rank]
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.f.read())) if len(r) >= 9]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), \
+            float(j["hbm_gbs"]), "measured"
+    return 1800.0, 1400.0, 6400.0, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per launch of the backward dK/dV kernel from the committed ncu
+    summary (None when absent or taken on an older kernel build)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        j = json.load(f)
+    return j.get("bwd_dkdv_bytes_per_launch")
+
+
+# -------------------------------------------------------------- reference
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle, timed on the host cores: each step is a bounded
+    sample (the median-length sequence of the batch, one KV head and its 4
+    query heads, forward + backward)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from diffusion_lm_block_bda_b300 import Problem, bda_attn_count_pairs
+    w, _ = rank_workload(1, 0)
+    inp = W.make_inputs(w, seed=0)
+    s = int(np.argsort(w.seqlens_q)[len(w.seqlens_q) // 2])
+    L = w.seqlens_q[s]
+    c = w.cu_seqlens_q
+    sl = slice(c[s], c[s + 1])
+    pairs = bda_attn_count_pairs(Problem([0, L], [0, L], 32, 8, 128, W.BLOCK_CAUSAL, 32))
+    G = w.hq // w.hkv
+    flops = 14.0 * w.head_dim * G * pairs
+    times = []
+    for i in range(args.warmup + args.steps):
+        kvh = i % w.hkv
+        t0 = time.perf_counter()
+        oracle.fwd_seq(w.kind, 32, L, inp["q"][sl], inp["k"][sl], inp["v"][sl], w.hq, w.hkv,
+                       w.softmax_scale, heads=(kvh * G, (kvh + 1) * G))
+        oracle.bwd_seq(w.kind, 32, L, inp["q"][sl], inp["k"][sl], inp["v"][sl], inp["dout"][sl],
+                       w.hq, w.hkv, w.softmax_scale, kv_heads=(kvh, kvh + 1))
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times)
+    value = flops * len(times) / t / 1e12
+    sample = (f"sequence {s} (L={L}) of the packed batch, one KV head and its {G} query heads, "
+              f"fwd+bwd fp64 per step")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1e3 * t / len(times), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16 inputs)",
+           "config": {"workload": WORKLOAD_NAME, "sample": sample},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def cpu_baseline(w, inp):
+    """The oracle as it stands on one bounded sample: the median-length
+    sequence, all heads, fwd+bwd."""
+    import numpy as np
+    import oracle
+    from diffusion_lm_block_bda_b300 import Problem, bda_attn_count_pairs
+    s = int(np.argsort(w.seqlens_q)[len(w.seqlens_q) // 2])
+    L = w.seqlens_q[s]
+    c = w.cu_seqlens_q
+    sl = slice(c[s], c[s + 1])
+    pairs = bda_attn_count_pairs(Problem([0, L], [0, L], w.hq, w.hkv, w.head_dim, w.kind,
+                                         w.block_size))
+    t0 = time.perf_counter()
+    oracle.fwd_seq(w.kind, w.block_size, L, inp["q"][sl], inp["k"][sl], inp["v"][sl], w.hq,
+                   w.hkv, w.softmax_scale)
+    oracle.bwd_seq(w.kind, w.block_size, L, inp["q"][sl], inp["k"][sl], inp["v"][sl],
+                   inp["dout"][sl], w.hq, w.hkv, w.softmax_scale)
+    t = time.perf_counter() - t0
+    flops = 14.0 * w.head_dim * w.hq * pairs
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"sequence {s} (L={L}) of the packed batch, all {w.hq} heads, fwd+bwd fp64, "
+                      f"{t:.1f} s"}
+
+
+# ------------------------------------------------------------------ native
+def main():
+    args = parse()
+    if args.impl == "reference":
+        # CPU-only arm: rank 0 runs the oracle, other ranks have nothing to do.
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        return
+    world, rank, local = dist_setup(args)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    import diffusion_lm_block_bda_b300 as bda
+    from diffusion_lm_block_bda_b300 import Problem
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w, seq_ids = rank_workload(world, rank)
+    inp = W.make_inputs(w, seed=rank)
+    pb = Problem.from_workload(w)
+    pairs = bda.bda_attn_count_pairs(pb)
+    d, hq = w.head_dim, w.hq
+    fwd_flops = 4.0 * d * hq * pairs
+    bwd_flops = 10.0 * d * hq * pairs
+    step_flops = fwd_flops + bwd_flops
+
+    q, k, v, dout = (inp[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o = torch.empty_like(q)
+    lse = torch.empty((hq, pb.total_q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.zeros(bda.bda_attn_workspace_size(pb, True), dtype=torch.uint8, device=dev)
+    n_plan = bda.bda_attn_plan_size(pb)
+    ring = [torch.empty(n_plan, dtype=torch.uint8).pin_memory() for _ in range(4)]
+    ring_ev = [None] * len(ring)
+    stream = torch.cuda.current_stream()
+    step_no = [0]
+
+    def plan():
+        b = step_no[0] % len(ring)
+        if ring_ev[b] is not None:
+            ring_ev[b].synchronize()  # the copy from this host buffer has run
+        bda.bda_attn_plan(pb, ring[b], ws, stream)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        ring_ev[b] = ev
+        step_no[0] += 1
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        plan()
+        if evs:
+            evs[1].record(stream)
+        bda.bda_attn_fwd(pb, q, k, v, o, lse, ws, stream)
+        if evs:
+            evs[2].record(stream)
+        bda.bda_attn_bwd_preprocess(pb, o, dout, ws, stream)
+        if evs:
+            evs[3].record(stream)
+        bda.bda_attn_bwd_dkdv(pb, q, k, v, lse, dout, dk, dv, ws, stream)
+        if evs:
+            evs[4].record(stream)
+        bda.bda_attn_bwd_dq_convert(pb, dq, ws, stream)
+        if evs:
+            evs[5].record(stream)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    clk = Clocks(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or local))
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if bda.bda_attn_check_status(ws, stream) != bda.BDA_OK:
+        raise SystemExit("device status reports a timeout during warm-up")
+
+    # ---- device-resident timed region
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = t0.elapsed_time(t1)
+    stage_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j in range(5)]
+    gpu_launches = 4 * K
+
+    # ---- end-to-end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: inp[n].pin_memory() for n in ("q", "k", "v", "dout")}
+        host_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                    "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
+                    "dq": torch.empty(dq.shape, dtype=dq.dtype).pin_memory(),
+                    "dk": torch.empty(dk.shape, dtype=dk.dtype).pin_memory(),
+                    "dv": torch.empty(dv.shape, dtype=dv.dtype).pin_memory()}
+        dev_in = {"q": q, "k": k, "v": v, "dout": dout}
+        dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for n, t in host_in.items():
+                dev_in[n].copy_(t, non_blocking=True)
+            step()
+            for n, t in host_out.items():
+                t.copy_(dev_out[n], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        K2 = max(3, min(K, 20))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(K2):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K2, world)
+        e2e_flops = sum_over_ranks(step_flops, world)
+        e2e = {"value": e2e_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K2,
+               "ms_per_step": e2e_ms}
+    clocks = clk.stop()
+    status = bda.bda_attn_check_status(ws, stream)
+    if status != bda.BDA_OK:
+        raise SystemExit(f"device status {status} after the timed region")
+
+    ms = max_over_ranks(total_ms / K, world)
+    total_flops = sum_over_ranks(step_flops, world)
+    value = total_flops / (ms * 1e-3) / 1e12
+    peak_burst, peak_sust, hbm, peak_kind = measured_peaks()
+    dkdv_ms = stage_ms[3]
+    achieved = bwd_flops / (dkdv_ms * 1e-3) / 1e12
+    stages = dict(zip(["plan", "fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"],
+                      [round(x, 4) for x in stage_ms]))
+
+    if rank != 0:
+        return
+    out = {
+        "impl": "native",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 inputs)",
+        "config": {"workload": WORKLOAD_NAME, "total_tokens": pb.total_q,
+                   "seqlens": w.seqlens_q, "useful_pairs_per_head": pairs,
+                   "useful_gflop_per_step": step_flops / 1e9,
+                   "l2": "inputs larger than L2 (Q, O, dO, dQ 0.3 GB each)",
+                   "parallelism": f"dp{world} (whole sequences, LPT-sharded)" if world > 1 else "1 GPU"},
+        "frac_of_peak": value / peak_burst,
+        "stages_ms": stages,
+        "roofline": {"kernel": "bda_bwd_dkdv", "bound": "tensor", "achieved": achieved,
+                     "peak": peak_burst, "unit": "TFLOP/s", "frac": achieved / peak_burst,
+                     "peak_kind": f"bf16 burst ({peak_kind})",
+                     "frac_of_sustained": achieved / peak_sust,
+                     "traffic": profiled_traffic()},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+    out["fwd_tflops"] = fwd_flops / (stage_ms[1] * 1e-3) / 1e12
+    out["bwd_tflops"] = bwd_flops / (sum(stage_ms[2:]) * 1e-3) / 1e12
+    if e2e is not None:
+        out["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, inp)
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()
