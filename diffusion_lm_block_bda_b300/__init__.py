@@ -34,7 +34,7 @@ EXPORTED = (
     "bda_attn_fwd",
     "bda_attn_bwd", "bda_attn_bwd_preprocess", "bda_attn_bwd_dkdv", "bda_attn_bwd_dq_convert",
     "bda_attn_count_pairs", "bda_attn_check_status", "bda_status_string",
-    "bda_last_cuda_error",
+    "bda_last_cuda_error", "bda_attn_fwd_noalloc",
 )
 
 
@@ -86,6 +86,7 @@ def lib():
             "bda_attn_check_status": ([vp, sz, st], ctypes.c_int),
             "bda_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "bda_last_cuda_error": ([], ctypes.c_char_p),
+            "bda_attn_fwd_noalloc": ([P, M, vp, vp, vp, vp, vp, st], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -186,6 +187,14 @@ def bda_attn_plan_host(pb: Problem, host_plan):
 def bda_attn_fwd(pb: Problem, q, k, v, o, lse, ws, stream=None):
     _check(lib().bda_attn_fwd(*pb.refs(), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws),
                               ws.numel(), _stream(stream)), "bda_attn_fwd")
+
+
+def bda_attn_fwd_noalloc(pb: Problem, q, k, v, o, lse, stream=None):
+    """Forward without a workspace (for callers that cannot allocate device
+    memory where they run attention): the plan lives in a fixed 1 MiB array
+    inside the library, shared by every call; overlapping calls race."""
+    _check(lib().bda_attn_fwd_noalloc(*pb.refs(), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                      _stream(stream)), "bda_attn_fwd_noalloc")
 
 
 def bda_attn_bwd(pb: Problem, q, k, v, o, lse, dout, dq, dk, dv, ws, stream=None):

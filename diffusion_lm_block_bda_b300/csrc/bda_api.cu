@@ -75,6 +75,9 @@ bda_status tensor_map_error() {
 const uint8_t* plan_ptr(const void* ws) { return static_cast<const uint8_t*>(ws); }
 
 }  // namespace
+
+void note_cuda_error(const char* text) { g_last_cuda_error = text; }
+
 }  // namespace bda
 
 using namespace bda;

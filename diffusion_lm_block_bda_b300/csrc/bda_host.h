@@ -34,4 +34,7 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
 
 long long count_pairs(const bda_problem* p, const bda_mask_desc* m, const Shape& s);
 
+// Records the text bda_last_cuda_error() returns on this thread.
+void note_cuda_error(const char* text);
+
 }  // namespace bda

@@ -159,6 +159,28 @@ long long bda_attn_count_pairs(const bda_problem *prob, const bda_mask_desc *mas
  * returns BDA_ERR_DEVICE_TIMEOUT if a kernel recorded a timeout. */
 bda_status bda_attn_check_status(void *ws, size_t ws_bytes, bda_stream_t stream);
 
+/* Forward without a workspace.  The paper has no counterpart: this entry
+ * exists for callers that cannot allocate device memory where they run
+ * attention -- e.g. a plugin inside an engine that owns all device memory
+ * through its own pool, or a decode loop that must not risk the device-wide
+ * synchronisation an allocation can cause.  Same arguments and results as
+ * bda_attn_fwd, minus the workspace: the tile plan and the status word live
+ * in a 1 MiB array compiled into the library (every GPU that loads the
+ * library holds it until the process exits), and the plan is built and
+ * copied on every call.  Allocates nothing (no cudaMalloc/cudaFree).
+ *   - BDA_ERR_WORKSPACE if the plan needs more than the 1 MiB array (about
+ *     16 thousand 128-row tiles); use bda_attn_fwd with a workspace then.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current); make it before any
+ *     stream capture begins on that device.
+ *   - Every call overwrites the shared array; calls whose GPU work overlaps
+ *     (other streams, other host threads) race on it and must be serialised
+ *     by the caller.  A device timeout is recorded in the array's status
+ *     word and is not readable through bda_attn_check_status. */
+bda_status bda_attn_fwd_noalloc(const bda_problem *prob, const bda_mask_desc *mask, const void *q,
+                                const void *k, const void *v, void *o, float *lse,
+                                bda_stream_t stream);
+
 const char *bda_status_string(bda_status s);
 
 /* Text of the CUDA error behind the most recent BDA_ERR_CUDA returned on the
