@@ -12,6 +12,7 @@
 #include "bda_host.h"
 #include "bda_internal.h"
 #include "bda_kernels.h"
+#include "bda_ptx.cuh"
 
 namespace bda {
 namespace {
@@ -271,7 +272,7 @@ bda_status bda_attn_check_status(void* ws, size_t ws_bytes, bda_stream_t stream)
   if (v == 0) return BDA_OK;
   if ((r = cuda_status(cudaMemsetAsync(ws, 0, sizeof(uint32_t), st))) != BDA_OK) return r;
   if ((r = cuda_status(cudaStreamSynchronize(st))) != BDA_OK) return r;
-  return BDA_ERR_DEVICE_TIMEOUT;
+  return (v & kDeviceTimeoutCode) ? BDA_ERR_DEVICE_TIMEOUT : BDA_ERR_UNSUPPORTED;
 }
 
 const char* bda_last_cuda_error(void) { return g_last_cuda_error; }

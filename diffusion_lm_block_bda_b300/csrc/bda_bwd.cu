@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(256) bda_dq_convert_kernel(const float* __rest
 constexpr int kBwdThreads = 320;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
 
+// Shared memory (D = 128): K | V | Q x2 | dO x2 | P-or-dS | LSE x2 | D x2 |
+// barriers = 226.1 KB, so there is no slack to align the base by hand: the
+// kernel checks that the dynamic shared memory starts 1024-byte aligned.
 template <int D>
 struct BwdLayout {
   static constexpr int CH = D / 64;
@@ -110,20 +113,19 @@ struct BwdLayout {
   static constexpr uint32_t PT = 2 * CHUNK;     // [128 keys][128 query cols] bf16
   static constexpr uint32_t K = 0;
   static constexpr uint32_t V = K + TILE;
-  static constexpr uint32_t Q = V + TILE;
-  static constexpr uint32_t DO = Q + TILE;
-  static constexpr uint32_t P = DO + TILE;
-  static constexpr uint32_t DS = P + PT;
-  static constexpr uint32_t LSE = DS + PT;      // float[128]: LSE * log2(e) per query col
-  static constexpr uint32_t DD = LSE + 512;     // float[128]: D per query col
-  static constexpr uint32_t BAR = DD + 512;
-  static constexpr int B_KV = 0, B_QFULL = 1, B_SFULL = 2, B_SFREE = 3, B_DPFULL = 4,
-                       B_DQFREE = 5, B_PFULL = 6, B_DSFULL = 7, B_DQFULL = 8, B_QEMPTY = 9,
-                       B_ACC = 10, NBAR = 11;
+  static constexpr uint32_t Q = V + TILE;       // 2 stages
+  static constexpr uint32_t DO = Q + 2 * TILE;  // 2 stages
+  static constexpr uint32_t PDS = DO + 2 * TILE;  // P^T, then dS^T of the same query tile
+  static constexpr uint32_t LSE = PDS + PT;     // float[2][128]: LSE * log2(e) per query col
+  static constexpr uint32_t DD = LSE + 1024;    // float[2][128]: D per query col
+  static constexpr uint32_t BAR = DD + 1024;
+  static constexpr int B_KV = 0, B_QFULL = 1 /* [2] */, B_QEMPTY = 3 /* [2] */, B_SFULL = 5,
+                       B_SFREE = 6, B_DPFULL = 7, B_DQFREE = 8, B_PFULL = 9, B_PCONS = 10,
+                       B_DSFULL = 11, B_DSCONS = 12, B_DQFULL = 13, B_ACC = 14, NBAR = 15;
   static constexpr uint32_t MISC = BAR + 8 * NBAR;
   static constexpr uint32_t BYTES = MISC + 16;
-  static constexpr uint32_t ALLOC = BYTES + 1024;
 };
+static_assert(BwdLayout<128>::BYTES <= 232448, "backward shared memory budget");
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
@@ -147,22 +149,32 @@ __device__ __forceinline__ void expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
+// Per (128-key tile, KV head) CTA; loops over the query tiles that see the
+// key tile.  MMA issue order per query tile i (one thread):
+//   dV_i += P_i^T dO_i          after P_i is in smem            -> PCONS
+//   S_{i+1}^T = K Q_{i+1}^T     after the softmax read S_i^T    -> SFULL
+//   dQ_i = dS_i K               after dS_i is in smem           -> DQFULL
+//   dK_i += dS_i^T Q_i                                          -> DSCONS, QEMPTY
+//   dP_{i+1}^T = V dO_{i+1}^T   after dQ_i left TMEM            -> DPFULL
+// MMAs into different accumulators are not ordered by the hardware, so every
+// reuse of a TMEM region or smem buffer waits for a commit of its readers.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                         const BwdArgs a) {
   using L = BwdLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  uint8_t* gbase = smem_raw;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (base & 1023u) {  // uniform across the CTA: nothing has been touched yet
+    if (tid == 0) atomicOr(a.status, kSmemAlignCode);
+    return;
+  }
   auto bar = [&](int i) -> uint32_t { return base + L::BAR + 8u * uint32_t(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::MISC + 4);
-  float* s_lse = reinterpret_cast<float*>(gbase + L::LSE);
-  float* s_D = reinterpret_cast<float*>(gbase + L::DD);
 
   const int item_idx = blockIdx.x / a.hkv;
   const int kvh = blockIdx.x - item_idx * a.hkv;
@@ -174,15 +186,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(bar(L::B_KV), 1);
-    mbar_init(bar(L::B_QFULL), 32);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::B_QFULL + s), 32);
+      mbar_init(bar(L::B_QEMPTY + s), 1);
+    }
     mbar_init(bar(L::B_SFULL), 1);
     mbar_init(bar(L::B_SFREE), 128);
     mbar_init(bar(L::B_DPFULL), 1);
     mbar_init(bar(L::B_DQFREE), 128);
     mbar_init(bar(L::B_PFULL), 128);
+    mbar_init(bar(L::B_PCONS), 1);
     mbar_init(bar(L::B_DSFULL), 128);
+    mbar_init(bar(L::B_DSCONS), 1);
     mbar_init(bar(L::B_DQFULL), 1);
-    mbar_init(bar(L::B_QEMPTY), 1);
     mbar_init(bar(L::B_ACC), 1);
     fence_mbar_init();
   }
@@ -195,14 +211,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const WaitCtx wc{abort_flag, a.status, a.timeout_ns};
-  // query tile i: token tile t0 (local) and head sub-group sub
+  // query tile i: token tile t0 (local) and head sub-group
   auto tile_t0 = [&](int i) -> int { return it.q_begin + (i / n_sub) * a.tok; };
   auto tile_h0 = [&](int i) -> int { return kvh * a.G + (i % n_sub) * a.hg; };
 
   bool ok = true;
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    int issued = 0;
+    int issued[2] = {0, 0};
     if (n_iter > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&tm_q);
@@ -216,16 +232,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       for (int i = 0; i < n_iter; ++i) {
-        if (i > 0 && !mbar_wait_warp(wc, bar(L::B_QEMPTY), uint32_t(i - 1) & 1u)) { ok = false; break; }
+        const int st = i & 1;
+        if (i >= 2 &&
+            !mbar_wait_warp(wc, bar(L::B_QEMPTY + st), uint32_t((i >> 1) - 1) & 1u)) {
+          ok = false;
+          break;
+        }
         const int t0 = tile_t0(i), h0 = tile_h0(i);
         if (lane == 0) {
-          expect_tx(bar(L::B_QFULL), 2 * L::TILE);
+          expect_tx(bar(L::B_QFULL + st), 2 * L::TILE);
           for (int c = 0; c < L::CH; ++c) {
-            tma_load_3d(base + L::Q + c * L::CHUNK, &tm_q, bar(L::B_QFULL), c * 64, h0, it.q_row + t0);
-            tma_load_3d(base + L::DO + c * L::CHUNK, &tm_do, bar(L::B_QFULL), c * 64, h0,
-                        it.q_row + t0);
+            tma_load_3d(base + L::Q + st * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + st),
+                        c * 64, h0, it.q_row + t0);
+            tma_load_3d(base + L::DO + st * L::TILE + c * L::CHUNK, &tm_do, bar(L::B_QFULL + st),
+                        c * 64, h0, it.q_row + t0);
           }
         }
+        float* s_lse = reinterpret_cast<float*>(gbase + L::LSE) + 128 * st;
+        float* s_D = reinterpret_cast<float*>(gbase + L::DD) + 128 * st;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int col = lane + 32 * k;
@@ -240,68 +264,94 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           s_lse[col] = lv;
           s_D[col] = dv;
         }
-        mbar_arrive(bar(L::B_QFULL));
-        ++issued;
+        mbar_arrive(bar(L::B_QFULL + st));
+        ++issued[st];
       }
-      if (!ok || *abort_flag) {
-        if (lane == 0) {
-          drain_wait(wc, bar(L::B_KV), 0);
-          if (issued) drain_wait(wc, bar(L::B_QFULL), uint32_t(issued - 1) & 1u);
-        }
+      if ((!ok || *abort_flag) && lane == 0) {
+        drain_wait(wc, bar(L::B_KV), 0);
+        for (int st = 0; st < 2; ++st)
+          if (issued[st]) drain_wait(wc, bar(L::B_QFULL + st), uint32_t(issued[st] - 1) & 1u);
       }
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0 && n_iter > 0) {
-      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
-      constexpr uint32_t idAcc = idesc_bf16(128, D, false, true);     // dV, dK
-      constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);       // dQ
-      ok = mbar_wait(wc, bar(L::B_KV), 0);
-      for (int i = 0; ok && i < n_iter; ++i) {
-        const uint32_t ph = uint32_t(i) & 1u, php = uint32_t(i - 1) & 1u;
-        if (!mbar_wait(wc, bar(L::B_QFULL), ph)) { ok = false; break; }
-        if (i > 0 && !mbar_wait(wc, bar(L::B_SFREE), php)) { ok = false; break; }
-        tc_fence_after();
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t idAcc = idesc_bf16(128, D, false, true);    // dV, dK
+      constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ
+      auto issue_s = [&](int i) {  // S_i^T = K Q_i^T
+        const uint32_t qa = base + L::Q + (i & 1) * L::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
           mma_ss(tbase + kColS, sdesc_sw128(base + L::K + off, 16, 1024),
-                 sdesc_sw128(base + L::Q + off, 16, 1024), idSS, kk > 0);
+                 sdesc_sw128(qa + off, 16, 1024), idSS, kk > 0);
         }
         mma_commit(bar(L::B_SFULL));
-        if (i > 0 && !mbar_wait(wc, bar(L::B_DQFREE), php)) { ok = false; break; }
-        tc_fence_after();
+      };
+      auto issue_dp = [&](int i) {  // dP_i^T = V dO_i^T
+        const uint32_t da = base + L::DO + (i & 1) * L::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
           mma_ss(tbase + kColDP, sdesc_sw128(base + L::V + off, 16, 1024),
-                 sdesc_sw128(base + L::DO + off, 16, 1024), idSS, kk > 0);
+                 sdesc_sw128(da + off, 16, 1024), idSS, kk > 0);
         }
         mma_commit(bar(L::B_DPFULL));
+      };
+      ok = mbar_wait(wc, bar(L::B_KV), 0) && mbar_wait(wc, bar(L::B_QFULL), 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int i = 0; ok && i < n_iter; ++i) {
+        const uint32_t ph = uint32_t(i) & 1u;
+        const int st = i & 1;
+        // dV += P^T dO
         if (!mbar_wait(wc, bar(L::B_PFULL), ph)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk) {
           const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColDV, sdesc_sw128(base + L::P + aoff, 16, 1024),
-                 sdesc_sw128(base + L::DO + 2048u * kk, L::CHUNK, 1024), idAcc,
+          mma_ss(tbase + kColDV, sdesc_sw128(base + L::PDS + aoff, 16, 1024),
+                 sdesc_sw128(base + L::DO + st * L::TILE + 2048u * kk, L::CHUNK, 1024), idAcc,
                  (i > 0 || kk > 0) ? 1u : 0u);
         }
+        mma_commit(bar(L::B_PCONS));
+        // next S^T as soon as its Q is in and this S^T has been read
+        if (i + 1 < n_iter) {
+          if (!mbar_wait(wc, bar(L::B_QFULL + (st ^ 1)), uint32_t((i + 1) >> 1) & 1u) ||
+              !mbar_wait(wc, bar(L::B_SFREE), ph)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(i + 1);
+        }
+        // dQ = dS K, then dK += dS^T Q
         if (!mbar_wait(wc, bar(L::B_DSFULL), ph)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTileM / 16; ++kk) {
-          const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColDK, sdesc_sw128(base + L::DS + aoff, 16, 1024),
-                 sdesc_sw128(base + L::Q + 2048u * kk, L::CHUNK, 1024), idAcc,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ss(tbase + kColDP, sdesc_sw128(base + L::DS + 2048u * kk, L::CHUNK, 1024),
+          mma_ss(tbase + kColDP, sdesc_sw128(base + L::PDS + 2048u * kk, L::CHUNK, 1024),
                  sdesc_sw128(base + L::K + 2048u * kk, L::CHUNK, 1024), idDQ, kk > 0);
         mma_commit(bar(L::B_DQFULL));
-        mma_commit(bar(L::B_QEMPTY));
+#pragma unroll
+        for (int kk = 0; kk < kTileM / 16; ++kk) {
+          const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+          mma_ss(tbase + kColDK, sdesc_sw128(base + L::PDS + aoff, 16, 1024),
+                 sdesc_sw128(base + L::Q + st * L::TILE + 2048u * kk, L::CHUNK, 1024), idAcc,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(L::B_DSCONS));
+        mma_commit(bar(L::B_QEMPTY + st));
+        // next dP^T once dQ has left the dP region
+        if (i + 1 < n_iter) {
+          if (!mbar_wait(wc, bar(L::B_DQFREE), ph)) { ok = false; break; }
+          tc_fence_after();
+          issue_dp(i + 1);
+        }
       }
       mma_commit(bar(L::B_ACC));
       drain_wait(wc, bar(L::B_ACC), 0);
@@ -314,22 +364,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int q_hi = min(kq.hi - delta, it.lq);  // local query tokens [kq.lo - delta, q_hi)
     const uint32_t lane_addr = tbase + (uint32_t(warp * 32) << 16);
     const float sl2 = a.scale_log2;
+    uint8_t* pds = gbase + L::PDS;
     for (int i = 0; i < n_iter; ++i) {
       const uint32_t ph = uint32_t(i) & 1u;
+      const int st = i & 1;
+      const float* s_lse = reinterpret_cast<const float*>(gbase + L::LSE) + 128 * st;
+      const float* s_D = reinterpret_cast<const float*>(gbase + L::DD) + 128 * st;
       const int t0 = tile_t0(i);
       const int lo_c = key_valid ? kq.lo - delta - t0 : 0;
       const int hi_c = key_valid ? q_hi - t0 : 0;
       const unsigned span = hi_c > lo_c ? unsigned(hi_c - lo_c) : 0u;
       const bool full = lo_c <= 0 && hi_c >= a.tok;
       // QFULL publishes the producer's LSE / D staging to these threads.
-      if (!mbar_wait_warp(wc, bar(L::B_QFULL), ph)) { ok = false; break; }
+      if (!mbar_wait_warp(wc, bar(L::B_QFULL + st), uint32_t(i >> 1) & 1u)) { ok = false; break; }
       if (!mbar_wait_warp(wc, bar(L::B_SFULL), ph)) { ok = false; break; }
       tc_fence_after();
       // P^T = exp(scale S^T - LSE), masked, 32 columns at a time; kept packed
-      // (bf16 pairs, the values the dV MMA sees) for dS, and stored into smem
-      // as the K-major A operand of dV += P^T dO.
+      // (bf16 pairs, the values the dV MMA sees) for dS.
       uint32_t pp[kTileM / 2];
-      uint8_t* sp = gbase + L::P;
 #pragma unroll
       for (int c = 0; c < kTileM / 32; ++c) {
         uint32_t rr[32];
@@ -350,19 +402,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           pp[16 * c + j] = pack_bf16x2(p0, p1);
         }
-#pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
-          const int u = 4 * c + u4;
-          *reinterpret_cast<uint4*>(sp + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =
-              make_uint4(pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
-        }
       }
+      // the shared P/dS buffer is free once dQ and dK of the previous tile ran
+      if (i > 0 && !mbar_wait_warp(wc, bar(L::B_DSCONS), uint32_t(i - 1) & 1u)) { ok = false; break; }
+#pragma unroll
+      for (int u = 0; u < kTileM / 8; ++u)
+        *reinterpret_cast<uint4*>(pds + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =
+            make_uint4(pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
       fence_proxy_async_smem();
       mbar_arrive(bar(L::B_PFULL));
-      // dS^T = P^T o (dP^T - D)
+      // dS^T = P^T o (dP^T - D), written over P^T once the dV MMA has read it
       if (!mbar_wait_warp(wc, bar(L::B_DPFULL), ph)) { ok = false; break; }
+      if (!mbar_wait_warp(wc, bar(L::B_PCONS), ph)) { ok = false; break; }
       tc_fence_after();
-      uint8_t* sds = gbase + L::DS;
 #pragma unroll
       for (int c = 0; c < kTileM / 32; ++c) {
         uint32_t rr[32];
@@ -382,7 +434,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pk[j] = pack_bf16x2(d0, d1);
           }
           const int u = 4 * c + u4;
-          *reinterpret_cast<uint4*>(sds + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =
+          *reinterpret_cast<uint4*>(pds + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
@@ -467,10 +519,10 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const CUtensorMap& tdo, const BwdArgs& a, int n_items, cudaStream_t stream) {
   using L = BwdLayout<D>;
   cudaError_t e = cudaFuncSetAttribute(bda_bwd_dkdv_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::ALLOC));
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::BYTES));
   if (e != cudaSuccess) return e;
   const unsigned grid = unsigned(n_items) * unsigned(a.hkv);
-  bda_bwd_dkdv_kernel<D><<<grid, kBwdThreads, L::ALLOC, stream>>>(tq, tk, tv, tdo, a);
+  bda_bwd_dkdv_kernel<D><<<grid, kBwdThreads, L::BYTES, stream>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 

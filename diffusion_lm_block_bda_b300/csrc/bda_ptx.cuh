@@ -2,8 +2,8 @@
 // bulk tensor copies), tcgen05 (TMEM allocation, MMA, loads/stores, fences).
 //
 // Every wait on an mbarrier is bounded: it polls with try_wait, and after a
-// time limit (from %globaltimer) it records BDA_DEVICE_TIMEOUT in the
-// caller's status word, raises the CTA-wide abort flag and returns false.
+// time limit (from %globaltimer) it sets the timeout bit of the caller's
+// status word, raises the CTA-wide abort flag and returns false.
 // Nothing here traps or asserts.
 #pragma once
 #include <cstdint>
@@ -11,7 +11,9 @@
 
 namespace bda {
 
-constexpr uint32_t kDeviceTimeoutCode = 5u;  // == BDA_ERR_DEVICE_TIMEOUT
+// Bits of the device status word in the workspace (bda_attn_check_status).
+constexpr uint32_t kDeviceTimeoutCode = 1u;  // a bounded wait ran out
+constexpr uint32_t kSmemAlignCode = 2u;      // dynamic shared memory not 1024-byte aligned
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -156,7 +156,9 @@ bda_status bda_attn_bwd_dq_convert(const bda_problem *prob, const bda_mask_desc 
 long long bda_attn_count_pairs(const bda_problem *prob, const bda_mask_desc *mask);
 
 /* Synchronises `stream`, reads the workspace status word, clears it, and
- * returns BDA_ERR_DEVICE_TIMEOUT if a kernel recorded a timeout. */
+ * returns BDA_ERR_DEVICE_TIMEOUT if a kernel recorded a timeout, or
+ * BDA_ERR_UNSUPPORTED if a kernel found its shared memory misaligned (the
+ * kernels then return without computing; never expected on sm_103a). */
 bda_status bda_attn_check_status(void *ws, size_t ws_bytes, bda_stream_t stream);
 
 /* Forward without a workspace.  The paper has no counterpart: this entry
