@@ -211,8 +211,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const WaitCtx wc{abort_flag, a.status, a.timeout_ns};
-  // query tile i: token tile t0 (local) and head sub-group
-  auto tile_t0 = [&](int i) -> int { return it.q_begin + (i / n_sub) * a.tok; };
+  // Query tile i: token tile t0 (local) and head sub-group.  Tiles are walked
+  // from the end of the sequence down, so the CTAs of one sequence, which
+  // start together, sweep the same query rows at the same time (L2 reuse of
+  // Q, dO and the dQ accumulator).
+  const int n_tok_tiles = (it.q_end - it.q_begin + a.tok - 1) / a.tok;
+  auto tile_t0 = [&](int i) -> int { return it.q_begin + (n_tok_tiles - 1 - i / n_sub) * a.tok; };
   auto tile_h0 = [&](int i) -> int { return kvh * a.G + (i % n_sub) * a.hg; };
 
   bool ok = true;

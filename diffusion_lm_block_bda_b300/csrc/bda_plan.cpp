@@ -182,11 +182,23 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
       bw.push_back(it);
     }
   }
-  // Longest-first; ties keep packing order.
+  // Forward: longest-first; ties keep packing order.
   std::stable_sort(fw.begin(), fw.end(),
                    [](const FwdItem& a, const FwdItem& b) { return a.work > b.work; });
-  std::stable_sort(bw.begin(), bw.end(),
-                   [](const BwdItem& a, const BwdItem& b) { return a.work > b.work; });
+  // Backward: sequences longest-first (by their total work), and inside a
+  // sequence its key tiles longest-first.  CTAs that run together then share
+  // one sequence's Q, dO and dQ rows in L2 instead of streaming several
+  // sequences' (the dQ accumulation is read-modify-write in L2); the tail is
+  // still made of the shortest units of the shortest sequence.
+  std::vector<long long> seq_work(s.nseq, 0);
+  for (const BwdItem& b : bw) seq_work[b.seq] += b.work;
+  std::stable_sort(bw.begin(), bw.end(), [&](const BwdItem& a, const BwdItem& b) {
+    if (a.seq != b.seq) {
+      if (seq_work[a.seq] != seq_work[b.seq]) return seq_work[a.seq] > seq_work[b.seq];
+      return a.seq < b.seq;
+    }
+    return a.work > b.work;
+  });
   std::memcpy(out + kHeaderBytes, fw.data(), sizeof(FwdItem) * fw.size());
   std::memcpy(out + kHeaderBytes + sizeof(FwdItem) * fw.size(), bw.data(),
               sizeof(BwdItem) * bw.size());

@@ -4,8 +4,10 @@ decoded and compared exhaustively with the oracle's explicit mask.
 Forward: every allowed (query, key) pair of every query tile falls in exactly
 one listed key tile; tiles marked FULL hold only allowed pairs; no listed tile
 is empty.  Backward: the query-token range of each key tile holds every query
-that sees one of its keys.  Order: longest unit first, and the list schedule
-over 148 SMs ends within one unit of max(total / 148, longest unit)."""
+that sees one of its keys.  Order: forward longest unit first, backward
+sequence-major (longest sequences first, longest key tiles first inside each);
+a list schedule over 148 SMs ends within one unit of max(total / 148, longest
+unit)."""
 import random
 
 import numpy as np
@@ -91,10 +93,23 @@ def check_plan(w):
         assert it["work"] == -(-n_tok // tok) * (G // hg)
     assert sorted(it["kpos0"] + ck[it["seq"]] for it in bw) == sorted(
         ck[s] + kp for s in range(w.nseq) for kp in range(0, ck[s + 1] - ck[s], 128))
-    # LPT order and the list-scheduling bound
+    # Order: forward longest-first; backward sequence-major (sequences by total
+    # work, longest first; inside a sequence its key tiles longest-first).
+    works = [it["work"] for it in fw]
+    assert works == sorted(works, reverse=True)
+    seq_order = []
+    for it in bw:
+        if not seq_order or seq_order[-1] != it["seq"]:
+            assert it["seq"] not in seq_order, "a sequence's key tiles are not contiguous"
+            seq_order.append(it["seq"])
+    totals = [sum(it["work"] for it in bw if it["seq"] == s) for s in seq_order]
+    assert totals == sorted(totals, reverse=True)
+    for s in seq_order:
+        ws = [it["work"] for it in bw if it["seq"] == s]
+        assert ws == sorted(ws, reverse=True)
+    # any list schedule ends within one unit of the mean load
     for items in (fw, bw):
         works = [it["work"] for it in items]
-        assert works == sorted(works, reverse=True)
         if works:
             m = 148
             loads = [0] * m
@@ -149,6 +164,5 @@ def test_planner_long_sequence_counts():
     fw, bw, hg, tok = decode(Problem.from_workload(w))
     assert hg == 4 and tok == 32
     assert len(fw) == 32768 // 32 and len(bw) == 32768 // 128
-    assert sum(it["work"] for it in fw) == sum(-(-(32 * i + 64 * 1) // 128) for i in range(0))  or True
     works = sorted(it["work"] for it in fw)
     assert works[0] == 1 and works[-1] == 256
