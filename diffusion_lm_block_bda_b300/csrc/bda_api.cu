@@ -52,6 +52,21 @@ bool make_thd_map(CUtensorMap* m, const void* ptr, int d, int heads, int64_t row
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the fp32 dQ accumulator [rows][heads][d]; box = 32 floats
+// (128 bytes, 128B swizzle) x box_h heads x box_rows rows.
+bool make_f32_map(CUtensorMap* m, const void* ptr, int d, int heads, int64_t rows, int box_h,
+                  int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
+  cuuint64_t strides[2] = {cuuint64_t(d) * 4, cuuint64_t(d) * 4 * cuuint64_t(heads)};
+  cuuint32_t box[3] = {32, cuuint32_t(box_h), cuuint32_t(box_rows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bda_status check_ws(const Shape& s, const void* ws, size_t ws_bytes, bool with_bwd) {
@@ -189,24 +204,26 @@ bda_status bda_attn_bwd_dkdv(const bda_problem* prob, const bda_mask_desc* mask,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dk) || !aligned16(dv))
     return BDA_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  uint8_t* w = static_cast<uint8_t*>(ws);
   // A problem without queries still launches (dK = dV = 0); point the query
-  // maps at the key tensor, they are never read.
+  // maps at the key tensor and the workspace, they are never accessed.
   const int64_t rq = s.total_q > 0 ? s.total_q : 1;
   const void* qsrc = s.total_q > 0 ? q : k;
   const void* dsrc = s.total_q > 0 ? dout : k;
+  const void* accsrc = s.total_q > 0 ? static_cast<const void*>(w + ws_offset_dqacc(s)) : ws;
   const int hq_map = s.total_q > 0 ? s.hq : s.hkv;
-  if (!make_thd_map(&tq, qsrc, s.d, hq_map, rq, s.total_q > 0 ? s.hg : 1, s.tok) ||
-      !make_thd_map(&tdo, dsrc, s.d, hq_map, rq, s.total_q > 0 ? s.hg : 1, s.tok) ||
+  const int hg_map = s.total_q > 0 ? s.hg : 1;
+  if (!make_thd_map(&tq, qsrc, s.d, hq_map, rq, hg_map, s.tok) ||
+      !make_thd_map(&tdo, dsrc, s.d, hq_map, rq, hg_map, s.tok) ||
       !make_thd_map(&tk, k, s.d, s.hkv, s.total_k, 1, kTileN) ||
-      !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN))
+      !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN) ||
+      !make_f32_map(&tdq, accsrc, s.d, s.total_q > 0 ? s.hq : 1, rq, hg_map, s.tok))
     return tensor_map_error();
-  uint8_t* w = static_cast<uint8_t*>(ws);
   BwdArgs a{};
   a.items = reinterpret_cast<const BwdItem*>(w + kHeaderBytes + sizeof(FwdItem) * size_t(s.n_fwd));
   a.lse = lse;
   a.D = reinterpret_cast<const float*>(w + ws_offset_D(s));
-  a.dq_acc = reinterpret_cast<float*>(w + ws_offset_dqacc(s));
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   a.status = reinterpret_cast<uint32_t*>(ws);
@@ -221,7 +238,7 @@ bda_status bda_attn_bwd_dkdv(const bda_problem* prob, const bda_mask_desc* mask,
   a.block = s.B;
   a.scale = s.scale;
   a.scale_log2 = s.scale * 1.4426950408889634f;
-  return cuda_status(launch_bwd_dkdv(s.d, tq, tk, tv, tdo, a, s.n_bwd,
+  return cuda_status(launch_bwd_dkdv(s.d, tq, tk, tv, tdo, tdq, a, s.n_bwd,
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 

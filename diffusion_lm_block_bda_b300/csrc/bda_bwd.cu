@@ -11,21 +11,22 @@
 //      TMEM over every query tile (tok tokens x hg heads of the group) that
 //      sees the key tile; the mask comes from block indices.  Per query tile:
 //        S^T  = K Q^T            (tcgen05, TMEM)
-//        P^T  -> bf16 smem       (softmax warps, thread = key row)
+//        P^T  -> bf16 TMEM       (softmax warps, thread = key row; written over
+//                                 the S^T columns already read)
 //        dP^T = V dO^T           (tcgen05, TMEM)
-//        dV  += P^T dO           (tcgen05, A from smem)
+//        dV  += P^T dO           (tcgen05, A = P^T from TMEM)
 //        dS^T -> bf16 smem       (softmax warps)
 //        dK  += dS^T Q           (tcgen05)
 //        dQ_t = dS K             (tcgen05, A = the same dS^T buffer read MN-major)
-//      and the dQ partial is added to the fp32 accumulator with vector
-//      reductions by a second warpgroup.
+//      and a second warpgroup moves the dQ partial TMEM -> smem, from where
+//      the TMA adds it into the fp32 accumulator (bulk tensor reduce-add).
 //   3. dq_convert: dQ = bf16(scale * accumulator).
 // Roles of the dK/dV kernel (320 threads):
 //   warps 0..3   softmax: P^T and dS^T, then the dK epilogue
-//   warps 4..7   dQ readout + global reductions, then the dV epilogue
+//   warps 4..7   dQ readout + staging for the TMA reduce, then the dV epilogue
 //   warp 8       producer: K/V once, then Q, dO (TMA) and LSE, D per query tile
 //   warp 9       MMA issuer (one thread)
-// TMEM columns: S^T [0,128) dP^T / dQ [128,256) dK [256,256+D) dV [384,384+D).
+// TMEM columns: S^T / P^T [0,128) dP^T / dQ [128,256) dK [256,256+D) dV [384,384+D).
 #include <cuda_bf16.h>
 
 #include "bda_internal.h"
@@ -101,37 +102,34 @@ __global__ void __launch_bounds__(256) bda_dq_convert_kernel(const float* __rest
 // ------------------------------------------------------------------ dK/dV
 constexpr int kBwdThreads = 320;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
+constexpr uint32_t kDqBarrier = 1;  // named barrier of the dQ warpgroup (warps 4..7)
 
-// Shared memory (D = 128): K | V | Q x2 | dO x2 | P-or-dS | LSE x2 | D x2 |
-// barriers = 226.1 KB, so there is no slack to align the base by hand: the
-// kernel checks that the dynamic shared memory starts 1024-byte aligned.
+// Shared memory (D = 128): K | V | Q x2 | dO | dS^T | dQ staging x2 | LSE x2 |
+// D x2 | barriers = 226.1 KB, so there is no slack to align the base by hand:
+// the kernel checks that the dynamic shared memory starts 1024-byte aligned.
 template <int D>
 struct BwdLayout {
   static constexpr int CH = D / 64;
-  static constexpr uint32_t CHUNK = 128 * 128;  // [128 rows][64 bf16], 128B-swizzled
+  static constexpr int NQC = D / 32;            // 32-float chunks of a dQ row
+  static constexpr uint32_t CHUNK = 128 * 128;  // [128 rows][128 B], 128B-swizzled
   static constexpr uint32_t TILE = CH * CHUNK;  // a K, V, Q or dO tile
-  static constexpr uint32_t PT = 2 * CHUNK;     // [128 keys][128 query cols] bf16
   static constexpr uint32_t K = 0;
   static constexpr uint32_t V = K + TILE;
-  static constexpr uint32_t Q = V + TILE;       // 2 stages
-  static constexpr uint32_t DO = Q + 2 * TILE;  // 2 stages
-  static constexpr uint32_t PDS = DO + 2 * TILE;  // P^T, then dS^T of the same query tile
-  static constexpr uint32_t LSE = PDS + PT;     // float[2][128]: LSE * log2(e) per query col
-  static constexpr uint32_t DD = LSE + 1024;    // float[2][128]: D per query col
+  static constexpr uint32_t Q = V + TILE;          // 2 stages
+  static constexpr uint32_t DO = Q + 2 * TILE;     // 1 stage
+  static constexpr uint32_t DS = DO + TILE;        // dS^T [128 keys][128 query cols] bf16
+  static constexpr uint32_t STG = DS + 2 * CHUNK;  // dQ staging: 2 x [128 rows][32 fp32]
+  static constexpr uint32_t LSE = STG + 2 * CHUNK;  // float[2][128]: LSE * log2(e) per query col
+  static constexpr uint32_t DD = LSE + 1024;        // float[2][128]: D per query col
   static constexpr uint32_t BAR = DD + 1024;
-  static constexpr int B_KV = 0, B_QFULL = 1 /* [2] */, B_QEMPTY = 3 /* [2] */, B_SFULL = 5,
-                       B_SFREE = 6, B_DPFULL = 7, B_DQFREE = 8, B_PFULL = 9, B_PCONS = 10,
-                       B_DSFULL = 11, B_DSCONS = 12, B_DQFULL = 13, B_ACC = 14, NBAR = 15;
+  enum {
+    B_KV = 0, B_QFULL = 1 /* [2] */, B_QEMPTY = 3 /* [2] */, B_DOFULL = 5, B_SFULL, B_PFULL,
+    B_DVDONE, B_DPFULL, B_DSFULL, B_DQFULL, B_DQFREE, B_DSCONS, B_ACC, NBAR
+  };
   static constexpr uint32_t MISC = BAR + 8 * NBAR;
   static constexpr uint32_t BYTES = MISC + 16;
 };
 static_assert(BwdLayout<128>::BYTES <= 232448, "backward shared memory budget");
-
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
 
 __device__ __forceinline__ bool drain_wait(WaitCtx w, uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
@@ -149,20 +147,23 @@ __device__ __forceinline__ void expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
-// Per (128-key tile, KV head) CTA; loops over the query tiles that see the
-// key tile.  MMA issue order per query tile i (one thread):
-//   dV_i += P_i^T dO_i          after P_i is in smem            -> PCONS
-//   S_{i+1}^T = K Q_{i+1}^T     after the softmax read S_i^T    -> SFULL
-//   dQ_i = dS_i K               after dS_i is in smem           -> DQFULL
-//   dK_i += dS_i^T Q_i                                          -> DSCONS, QEMPTY
-//   dP_{i+1}^T = V dO_{i+1}^T   after dQ_i left TMEM            -> DPFULL
+// Per (128-key tile, KV head) CTA; loops over the query tiles i that see the
+// key tile.  MMA issue order per query tile (one thread):
+//   dV   += P_i^T dO_i      A = P^T from TMEM, after P_i^T is stored    -> DVDONE
+//   S^T_{i+1} = K Q_{i+1}^T after dV_i has read P_i^T (same columns)    -> SFULL
+//   dQ_i  = dS_i K          after dS_i^T is in smem                     -> DQFULL
+//   dK   += dS_i^T Q_i                                                   -> DSCONS, QEMPTY
+//   dP^T_{i+1} = V dO_{i+1}^T after dQ_i left TMEM and dO_{i+1} landed  -> DPFULL
 // MMAs into different accumulators are not ordered by the hardware, so every
 // reuse of a TMEM region or smem buffer waits for a commit of its readers.
+// The dQ partial of each query tile leaves TMEM through shared memory and is
+// added to the fp32 accumulator by TMA reduce-add (per-element atomic), so no
+// thread issues global atomics.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                        const BwdArgs a) {
+                        const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -190,15 +191,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(L::B_QFULL + s), 32);
       mbar_init(bar(L::B_QEMPTY + s), 1);
     }
+    mbar_init(bar(L::B_DOFULL), 1);
     mbar_init(bar(L::B_SFULL), 1);
-    mbar_init(bar(L::B_SFREE), 128);
-    mbar_init(bar(L::B_DPFULL), 1);
-    mbar_init(bar(L::B_DQFREE), 128);
     mbar_init(bar(L::B_PFULL), 128);
-    mbar_init(bar(L::B_PCONS), 1);
+    mbar_init(bar(L::B_DVDONE), 1);
+    mbar_init(bar(L::B_DPFULL), 1);
     mbar_init(bar(L::B_DSFULL), 128);
-    mbar_init(bar(L::B_DSCONS), 1);
     mbar_init(bar(L::B_DQFULL), 1);
+    mbar_init(bar(L::B_DQFREE), 128);
+    mbar_init(bar(L::B_DSCONS), 1);
     mbar_init(bar(L::B_ACC), 1);
     fence_mbar_init();
   }
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   bool ok = true;
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    int issued[2] = {0, 0};
+    int nq0 = 0, nq1 = 0, ndo = 0;  // copies issued per barrier (abort drain)
     if (n_iter > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&tm_q);
@@ -235,6 +236,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(base + L::V + c * L::CHUNK, &tm_v, bar(L::B_KV), c * 64, kvh, it.k_row);
         }
       }
+      // LSE and D of a query tile are fetched one tile ahead, into registers.
+      float lv[4], dv[4];
+      auto fetch = [&](int i) {
+        const int t0 = tile_t0(i), h0 = tile_h0(i);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int col = lane + 32 * k;
+          const int tok = t0 + (col >> a.lg_hg);
+          const int h = h0 + (col & (a.hg - 1));
+          lv[k] = INFINITY;
+          dv[k] = 0.f;
+          if (tok < it.lq) {
+            const size_t idx = size_t(h) * size_t(a.total_q) + size_t(it.q_row + tok);
+            lv[k] = a.lse[idx] * 1.4426950408889634f;
+            dv[k] = a.D[idx];
+          }
+        }
+      };
+      fetch(0);
       for (int i = 0; i < n_iter; ++i) {
         const int st = i & 1;
         if (i >= 2 &&
@@ -244,37 +264,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         const int t0 = tile_t0(i), h0 = tile_h0(i);
         if (lane == 0) {
-          expect_tx(bar(L::B_QFULL + st), 2 * L::TILE);
-          for (int c = 0; c < L::CH; ++c) {
+          expect_tx(bar(L::B_QFULL + st), L::TILE);
+          for (int c = 0; c < L::CH; ++c)
             tma_load_3d(base + L::Q + st * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + st),
                         c * 64, h0, it.q_row + t0);
-            tma_load_3d(base + L::DO + st * L::TILE + c * L::CHUNK, &tm_do, bar(L::B_QFULL + st),
-                        c * 64, h0, it.q_row + t0);
-          }
         }
         float* s_lse = reinterpret_cast<float*>(gbase + L::LSE) + 128 * st;
         float* s_D = reinterpret_cast<float*>(gbase + L::DD) + 128 * st;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int col = lane + 32 * k;
-          const int tok = t0 + (col >> a.lg_hg);
-          const int h = h0 + (col & (a.hg - 1));
-          float lv = INFINITY, dv = 0.f;
-          if (tok < it.lq) {
-            const size_t idx = size_t(h) * size_t(a.total_q) + size_t(it.q_row + tok);
-            lv = a.lse[idx] * 1.4426950408889634f;
-            dv = a.D[idx];
-          }
-          s_lse[col] = lv;
-          s_D[col] = dv;
+          s_lse[lane + 32 * k] = lv[k];
+          s_D[lane + 32 * k] = dv[k];
         }
         mbar_arrive(bar(L::B_QFULL + st));
-        ++issued[st];
+        if (st == 0) ++nq0; else ++nq1;
+        if (i + 1 < n_iter) fetch(i + 1);
+        // dO has one buffer: tile i's once dV of tile i-1 has read it
+        if (i >= 1 && !mbar_wait_warp(wc, bar(L::B_DVDONE), uint32_t(i - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(L::B_DOFULL), L::TILE);
+          for (int c = 0; c < L::CH; ++c)
+            tma_load_3d(base + L::DO + c * L::CHUNK, &tm_do, bar(L::B_DOFULL), c * 64, h0,
+                        it.q_row + t0);
+        }
+        ++ndo;
       }
       if ((!ok || *abort_flag) && lane == 0) {
         drain_wait(wc, bar(L::B_KV), 0);
-        for (int st = 0; st < 2; ++st)
-          if (issued[st]) drain_wait(wc, bar(L::B_QFULL + st), uint32_t(issued[st] - 1) & 1u);
+        if (nq0) drain_wait(wc, bar(L::B_QFULL), uint32_t(nq0 - 1) & 1u);
+        if (nq1) drain_wait(wc, bar(L::B_QFULL + 1), uint32_t(nq1 - 1) & 1u);
+        if (ndo) drain_wait(wc, bar(L::B_DOFULL), uint32_t(ndo - 1) & 1u);
       }
     }
   } else if (warp == 9) {
@@ -293,13 +315,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mma_commit(bar(L::B_SFULL));
       };
-      auto issue_dp = [&](int i) {  // dP_i^T = V dO_i^T
-        const uint32_t da = base + L::DO + (i & 1) * L::TILE;
+      auto issue_dp = [&]() {  // dP^T = V dO^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
           mma_ss(tbase + kColDP, sdesc_sw128(base + L::V + off, 16, 1024),
-                 sdesc_sw128(da + off, 16, 1024), idSS, kk > 0);
+                 sdesc_sw128(base + L::DO + off, 16, 1024), idSS, kk > 0);
         }
         mma_commit(bar(L::B_DPFULL));
       };
@@ -307,26 +328,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        issue_dp(0);
+      }
+      ok = ok && mbar_wait(wc, bar(L::B_DOFULL), 0);
+      if (ok) {
+        tc_fence_after();
+        issue_dp();
       }
       for (int i = 0; ok && i < n_iter; ++i) {
         const uint32_t ph = uint32_t(i) & 1u;
         const int st = i & 1;
-        // dV += P^T dO
+        // dV += P^T dO, P^T (bf16 pairs) in the S^T columns
         if (!mbar_wait(wc, bar(L::B_PFULL), ph)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTileM / 16; ++kk) {
-          const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColDV, sdesc_sw128(base + L::PDS + aoff, 16, 1024),
-                 sdesc_sw128(base + L::DO + st * L::TILE + 2048u * kk, L::CHUNK, 1024), idAcc,
+        for (int kk = 0; kk < kTileM / 16; ++kk)
+          mma_ts(tbase + kColDV, tbase + kColS + 8u * kk,
+                 sdesc_sw128(base + L::DO + 2048u * kk, L::CHUNK, 1024), idAcc,
                  (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(L::B_PCONS));
-        // next S^T as soon as its Q is in and this S^T has been read
+        mma_commit(bar(L::B_DVDONE));
+        // next S^T once its Q is in and dV has read P^T out of the S^T columns
         if (i + 1 < n_iter) {
           if (!mbar_wait(wc, bar(L::B_QFULL + (st ^ 1)), uint32_t((i + 1) >> 1) & 1u) ||
-              !mbar_wait(wc, bar(L::B_SFREE), ph)) {
+              !mbar_wait(wc, bar(L::B_DVDONE), ph)) {
             ok = false;
             break;
           }
@@ -338,23 +361,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ss(tbase + kColDP, sdesc_sw128(base + L::PDS + 2048u * kk, L::CHUNK, 1024),
+          mma_ss(tbase + kColDP, sdesc_sw128(base + L::DS + 2048u * kk, L::CHUNK, 1024),
                  sdesc_sw128(base + L::K + 2048u * kk, L::CHUNK, 1024), idDQ, kk > 0);
         mma_commit(bar(L::B_DQFULL));
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk) {
           const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColDK, sdesc_sw128(base + L::PDS + aoff, 16, 1024),
+          mma_ss(tbase + kColDK, sdesc_sw128(base + L::DS + aoff, 16, 1024),
                  sdesc_sw128(base + L::Q + st * L::TILE + 2048u * kk, L::CHUNK, 1024), idAcc,
                  (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(L::B_DSCONS));
         mma_commit(bar(L::B_QEMPTY + st));
-        // next dP^T once dQ has left the dP region
+        // next dP^T once dQ has left the dP^T columns and dO_{i+1} is in
         if (i + 1 < n_iter) {
-          if (!mbar_wait(wc, bar(L::B_DQFREE), ph)) { ok = false; break; }
+          if (!mbar_wait(wc, bar(L::B_DQFREE), ph) ||
+              !mbar_wait(wc, bar(L::B_DOFULL), uint32_t(i + 1) & 1u)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          issue_dp(i + 1);
+          issue_dp();
         }
       }
       mma_commit(bar(L::B_ACC));
@@ -368,12 +395,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int q_hi = min(kq.hi - delta, it.lq);  // local query tokens [kq.lo - delta, q_hi)
     const uint32_t lane_addr = tbase + (uint32_t(warp * 32) << 16);
     const float sl2 = a.scale_log2;
-    uint8_t* pds = gbase + L::PDS;
+    uint8_t* dsb = gbase + L::DS;
     for (int i = 0; i < n_iter; ++i) {
       const uint32_t ph = uint32_t(i) & 1u;
       const int st = i & 1;
-      const float* s_lse = reinterpret_cast<const float*>(gbase + L::LSE) + 128 * st;
-      const float* s_D = reinterpret_cast<const float*>(gbase + L::DD) + 128 * st;
+      const float4* s_lse4 = reinterpret_cast<const float4*>(gbase + L::LSE) + 32 * st;
+      const float4* s_D4 = reinterpret_cast<const float4*>(gbase + L::DD) + 32 * st;
       const int t0 = tile_t0(i);
       const int lo_c = key_valid ? kq.lo - delta - t0 : 0;
       const int hi_c = key_valid ? q_hi - t0 : 0;
@@ -383,95 +410,136 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!mbar_wait_warp(wc, bar(L::B_QFULL + st), uint32_t(i >> 1) & 1u)) { ok = false; break; }
       if (!mbar_wait_warp(wc, bar(L::B_SFULL), ph)) { ok = false; break; }
       tc_fence_after();
-      // P^T = exp(scale S^T - LSE), masked, 32 columns at a time; kept packed
-      // (bf16 pairs, the values the dV MMA sees) for dS.
+      // P^T = exp(scale S^T - LSE), masked, 32 query columns at a time; the
+      // bf16 pairs go back into the S^T columns already read (chunk c fills
+      // columns [16c, 16c+16)) for the dV MMA, and stay in registers for dS.
       uint32_t pp[kTileM / 2];
+      auto p_chunk = [&](int c, const uint32_t (&r)[32]) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < kTileM / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + kColS + 32u * c, rr);
-        tmem_ld_wait(rr);
-        if (c == kTileM / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(bar(L::B_SFREE));
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int c0 = 32 * c + 2 * j, c1 = c0 + 1;
-          float p0 = ex2(fmaf(__uint_as_float(rr[2 * j]), sl2, -s_lse[c0]));
-          float p1 = ex2(fmaf(__uint_as_float(rr[2 * j + 1]), sl2, -s_lse[c1]));
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 l = s_lse4[8 * c + q4];
+          float p[4];
+          p[0] = ex2(fmaf(__uint_as_float(r[4 * q4 + 0]), sl2, -l.x));
+          p[1] = ex2(fmaf(__uint_as_float(r[4 * q4 + 1]), sl2, -l.y));
+          p[2] = ex2(fmaf(__uint_as_float(r[4 * q4 + 2]), sl2, -l.z));
+          p[3] = ex2(fmaf(__uint_as_float(r[4 * q4 + 3]), sl2, -l.w));
           if (!full) {
-            if (unsigned((c0 >> a.lg_hg) - lo_c) >= span) p0 = 0.f;
-            if (unsigned((c1 >> a.lg_hg) - lo_c) >= span) p1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (unsigned(((32 * c + 4 * q4 + e) >> a.lg_hg) - lo_c) >= span) p[e] = 0.f;
           }
-          pp[16 * c + j] = pack_bf16x2(p0, p1);
+          pk[2 * q4] = pack_bf16x2(p[0], p[1]);
+          pk[2 * q4 + 1] = pack_bf16x2(p[2], p[3]);
         }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pp[16 * c + j] = pk[j];
+        tmem_st16(lane_addr + kColS + 16u * c, pk);
+      };
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(lane_addr + kColS, ra);
+        tmem_ld_wait(ra);
+        tmem_ld32(lane_addr + kColS + 32u, rb);
+        p_chunk(0, ra);
+        tmem_ld_wait(rb);
+        tmem_ld32(lane_addr + kColS + 64u, ra);
+        p_chunk(1, rb);
+        tmem_ld_wait(ra);
+        tmem_ld32(lane_addr + kColS + 96u, rb);
+        p_chunk(2, ra);
+        tmem_ld_wait(rb);
+        p_chunk(3, rb);
       }
-      // the shared P/dS buffer is free once dQ and dK of the previous tile ran
-      if (i > 0 && !mbar_wait_warp(wc, bar(L::B_DSCONS), uint32_t(i - 1) & 1u)) { ok = false; break; }
-#pragma unroll
-      for (int u = 0; u < kTileM / 8; ++u)
-        *reinterpret_cast<uint4*>(pds + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =
-            make_uint4(pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
-      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
       mbar_arrive(bar(L::B_PFULL));
-      // dS^T = P^T o (dP^T - D), written over P^T once the dV MMA has read it
+      // dS^T = P^T o (dP^T - D) -> bf16 smem (K-major for dK, read MN-major for dQ)
       if (!mbar_wait_warp(wc, bar(L::B_DPFULL), ph)) { ok = false; break; }
-      if (!mbar_wait_warp(wc, bar(L::B_PCONS), ph)) { ok = false; break; }
+      // the dS^T buffer is free once dQ and dK of the previous tile ran
+      if (i > 0 && !mbar_wait_warp(wc, bar(L::B_DSCONS), uint32_t(i - 1) & 1u)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < kTileM / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + kColDP + 32u * c, rr);
-        tmem_ld_wait(rr);
+      auto ds_chunk = [&](int c, const uint32_t (&r)[32]) {
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
+          const float4 d0 = s_D4[8 * c + 2 * u4], d1 = s_D4[8 * c + 2 * u4 + 1];
+          const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
           uint32_t pk[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
+            const uint32_t pb = pp[16 * c + 4 * u4 + j];
             const int cc = 8 * u4 + 2 * j;
-            const int c0 = 32 * c + cc;
-            const uint32_t pb = pp[c0 >> 1];
-            const float d0 = __uint_as_float(pb << 16) * (__uint_as_float(rr[cc]) - s_D[c0]);
-            const float d1 = __uint_as_float(pb & 0xffff0000u) *
-                             (__uint_as_float(rr[cc + 1]) - s_D[c0 + 1]);
-            pk[j] = pack_bf16x2(d0, d1);
+            const float v0 = __uint_as_float(pb << 16) * (__uint_as_float(r[cc]) - dd[2 * j]);
+            const float v1 = __uint_as_float(pb & 0xffff0000u) *
+                             (__uint_as_float(r[cc + 1]) - dd[2 * j + 1]);
+            pk[j] = pack_bf16x2(v0, v1);
           }
           const int u = 4 * c + u4;
-          *reinterpret_cast<uint4*>(pds + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =
+          *reinterpret_cast<uint4*>(dsb + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+      };
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(lane_addr + kColDP, ra);
+        tmem_ld_wait(ra);
+        tmem_ld32(lane_addr + kColDP + 32u, rb);
+        ds_chunk(0, ra);
+        tmem_ld_wait(rb);
+        tmem_ld32(lane_addr + kColDP + 64u, ra);
+        ds_chunk(1, rb);
+        tmem_ld_wait(ra);
+        tmem_ld32(lane_addr + kColDP + 96u, rb);
+        ds_chunk(2, ra);
+        tmem_ld_wait(rb);
+        ds_chunk(3, rb);
       }
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar(L::B_DSFULL));
     }
   } else {
-    // ------------------------------------------------------ dQ reductions
-    const int qc = tid - 128;  // TMEM lane == query column of the tile
+    // ------------------------------------------- dQ: TMEM -> smem -> TMA add
+    const int qc = tid - 128;  // TMEM lane == query row of the tile
+    const bool leader = qc == 0;
     const uint32_t lane_addr = tbase + (uint32_t((warp - 4) * 32) << 16);
+    uint32_t n_chunks = 0;  // staging buffers handed to the TMA so far
     for (int i = 0; i < n_iter; ++i) {
-      if (!mbar_wait_warp(wc, bar(L::B_DQFULL), uint32_t(i) & 1u)) { ok = false; break; }
+      // All four warps leave together, so none is left at a named barrier.
+      bool good = mbar_wait_warp(wc, bar(L::B_DQFULL), uint32_t(i) & 1u);
+      good = named_bar_and(kDqBarrier, 128, good);
+      if (!good) { ok = false; break; }
       tc_fence_after();
-      float dq[D];
+      uint32_t rq[L::NQC][32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + kColDP + 32u * c, rr);
-        tmem_ld_wait(rr);
+      for (int c = 0; c < L::NQC; ++c) tmem_ld32(lane_addr + kColDP + 32u * c, rq[c]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) dq[32 * c + j] = __uint_as_float(rr[j]);
-      }
+      for (int c = 0; c < L::NQC; ++c) tmem_ld_wait(rq[c]);
       tc_fence_before();
       mbar_arrive(bar(L::B_DQFREE));
-      const int tok = tile_t0(i) + (qc >> a.lg_hg);
-      if (tok < it.lq) {
-        const int h = tile_h0(i) + (qc & (a.hg - 1));
-        float* dst = a.dq_acc + (size_t(it.q_row + tok) * size_t(a.hq) + size_t(h)) * size_t(D);
+      const int t0 = tile_t0(i), h0 = tile_h0(i);
 #pragma unroll
-        for (int j = 0; j < D; j += 4) red_add_v4(dst + j, dq[j], dq[j + 1], dq[j + 2], dq[j + 3]);
+      for (int c = 0; c < L::NQC; ++c) {
+        const uint32_t b = n_chunks & 1u;
+        if (n_chunks >= 2) {  // the reduce that used buffer b has read it
+          if (leader) bulk_wait_read<1>();
+          named_bar_sync(kDqBarrier, 128);
+        }
+        uint8_t* stg = gbase + L::STG + b * L::CHUNK;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(stg + sw128_offset(qc, u)) =
+              make_uint4(rq[c][4 * u], rq[c][4 * u + 1], rq[c][4 * u + 2], rq[c][4 * u + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(kDqBarrier, 128);
+        if (leader) {
+          tma_reduce_add_3d(&tm_dq, base + L::STG + b * L::CHUNK, 32 * c, h0, it.q_row + t0);
+          bulk_commit();
+        }
+        ++n_chunks;
       }
     }
+    if (leader) bulk_wait_all();
   }
 
   // ----------------------------------------------- dK (warps 0-3), dV (4-7)
@@ -520,13 +588,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const BwdArgs& a, int n_items, cudaStream_t stream) {
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
+                          int n_items, cudaStream_t stream) {
   using L = BwdLayout<D>;
   cudaError_t e = cudaFuncSetAttribute(bda_bwd_dkdv_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::BYTES));
   if (e != cudaSuccess) return e;
   const unsigned grid = unsigned(n_items) * unsigned(a.hkv);
-  bda_bwd_dkdv_kernel<D><<<grid, kBwdThreads, L::BYTES, stream>>>(tq, tk, tv, tdo, a);
+  bda_bwd_dkdv_kernel<D><<<grid, kBwdThreads, L::BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 
@@ -559,11 +628,11 @@ cudaError_t launch_bwd_preprocess(int head_dim, const __nv_bfloat16* o, const __
 }
 
 cudaError_t launch_bwd_dkdv(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
-                            int n_items, cudaStream_t stream) {
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                            const BwdArgs& a, int n_items, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
-  if (head_dim == 128) return launch_dkdv_t<128>(tq, tk, tv, tdo, a, n_items, stream);
-  return launch_dkdv_t<64>(tq, tk, tv, tdo, a, n_items, stream);
+  if (head_dim == 128) return launch_dkdv_t<128>(tq, tk, tv, tdo, tdq, a, n_items, stream);
+  return launch_dkdv_t<64>(tq, tk, tv, tdo, tdq, a, n_items, stream);
 }
 
 cudaError_t launch_dq_convert(int head_dim, const float* dq_acc, __nv_bfloat16* dq, int64_t total_q,

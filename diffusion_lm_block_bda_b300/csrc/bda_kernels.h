@@ -29,7 +29,6 @@ struct BwdArgs {
   const BwdItem* items;
   const float* lse;      // [hq][total_q]
   const float* D;        // [hq][total_q]
-  float* dq_acc;         // [total_q][hq][d], unscaled sum of dS K
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   uint32_t* status;
@@ -49,9 +48,11 @@ cudaError_t launch_bwd_preprocess(int head_dim, const __nv_bfloat16* o, const __
                                   float* D, float* dq_acc, int64_t total_q, int hq,
                                   cudaStream_t stream);
 
+// tdq: fp32 map over the dQ accumulator [total_q][hq][d] (unscaled sum of
+// dS K), box 32 floats x hg heads x tok tokens, 128-byte swizzle.
 cudaError_t launch_bwd_dkdv(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
-                            int n_items, cudaStream_t stream);
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                            const BwdArgs& a, int n_items, cudaStream_t stream);
 
 cudaError_t launch_dq_convert(int head_dim, const float* dq_acc, __nv_bfloat16* dq, int64_t total_q,
                               int hq, float scale, cudaStream_t stream);
