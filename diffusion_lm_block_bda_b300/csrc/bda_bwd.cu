@@ -404,8 +404,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int t0 = tile_t0(i);
       const int lo_c = key_valid ? kq.lo - delta - t0 : 0;
       const int hi_c = key_valid ? q_hi - t0 : 0;
-      const unsigned span = hi_c > lo_c ? unsigned(hi_c - lo_c) : 0u;
-      const bool full = lo_c <= 0 && hi_c >= a.tok;
+      // Visible query columns of this key row: [c_lo, c_hi) (column = token
+      // * hg + head).  Warps whose rows all see the whole tile skip masking.
+      const int c_lo = max(lo_c, 0) << a.lg_hg;
+      const int c_hi = hi_c <= lo_c ? c_lo : min(hi_c, a.tok) << a.lg_hg;
+      const bool warp_full = __all_sync(0xffffffffu, c_lo == 0 && c_hi >= kTileM);
       // QFULL publishes the producer's LSE / D staging to these threads.
       if (!mbar_wait_warp(wc, bar(L::B_QFULL + st), uint32_t(i >> 1) & 1u)) { ok = false; break; }
       if (!mbar_wait_warp(wc, bar(L::B_SFULL), ph)) { ok = false; break; }
@@ -419,18 +422,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
           const float4 l = s_lse4[8 * c + q4];
-          float p[4];
-          p[0] = ex2(fmaf(__uint_as_float(r[4 * q4 + 0]), sl2, -l.x));
-          p[1] = ex2(fmaf(__uint_as_float(r[4 * q4 + 1]), sl2, -l.y));
-          p[2] = ex2(fmaf(__uint_as_float(r[4 * q4 + 2]), sl2, -l.z));
-          p[3] = ex2(fmaf(__uint_as_float(r[4 * q4 + 3]), sl2, -l.w));
-          if (!full) {
+          const float p0 = ex2(fmaf(__uint_as_float(r[4 * q4 + 0]), sl2, -l.x));
+          const float p1 = ex2(fmaf(__uint_as_float(r[4 * q4 + 1]), sl2, -l.y));
+          const float p2 = ex2(fmaf(__uint_as_float(r[4 * q4 + 2]), sl2, -l.z));
+          const float p3 = ex2(fmaf(__uint_as_float(r[4 * q4 + 3]), sl2, -l.w));
+          pk[2 * q4] = pack_bf16x2(p0, p1);
+          pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
+        }
+        // Masking clears the bf16 halves of hidden columns.  It sits apart
+        // from the exponentials: a branch between them would keep the
+        // scheduler from overlapping their latencies.
+        if (!warp_full) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (unsigned(((32 * c + 4 * q4 + e) >> a.lg_hg) - lo_c) >= span) p[e] = 0.f;
+          for (int j = 0; j < 16; ++j) {
+            const int col = 32 * c + 2 * j;
+            const uint32_t lo = (col >= c_lo && col < c_hi) ? 0x0000ffffu : 0u;
+            const uint32_t hi = (col + 1 >= c_lo && col + 1 < c_hi) ? 0xffff0000u : 0u;
+            pk[j] &= lo | hi;
           }
-          pk[2 * q4] = pack_bf16x2(p[0], p[1]);
-          pk[2 * q4 + 1] = pack_bf16x2(p[2], p[3]);
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) pp[16 * c + j] = pk[j];
