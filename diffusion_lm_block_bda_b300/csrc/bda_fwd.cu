@@ -17,7 +17,9 @@
 //                 PARTIAL tiles from block indices, online max/sum, writes P
 //                 as bf16 into TMEM, rescales O when the max grows by more
 //                 than 2^8, and runs the epilogue (O / l, LSE).
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+D) P [384,448).
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+D) P0 [384,448) P1 [448,512).
+// S and P are both double buffered, so the softmax of tile n+1 overlaps the
+// P V product of tile n; it waits for that product only to rescale O.
 #include <cuda_bf16.h>
 
 #include "bda_internal.h"
@@ -29,7 +31,7 @@ namespace bda {
 namespace {
 
 constexpr int kFwdThreads = 192;
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // P0 at kColP, P1 at kColP + 64
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
 
 template <int D, int NST>
@@ -42,7 +44,7 @@ struct FwdLayout {
   static constexpr uint32_t V = K + NST * TILE;
   static constexpr uint32_t BAR = V + NST * TILE;
   // q_full, k_full[NST], k_empty[NST], v_full[NST], v_empty[NST],
-  // s_full[2], s_free[2], p_full, o_done, drain
+  // s_full[2], s_free[2], p_full, o_done[2] (per P buffer), drain
   static constexpr int B_QFULL = 0;
   static constexpr int B_KFULL = 1;
   static constexpr int B_KEMPTY = B_KFULL + NST;
@@ -52,7 +54,7 @@ struct FwdLayout {
   static constexpr int B_SFREE = B_SFULL + 2;
   static constexpr int B_PFULL = B_SFREE + 2;
   static constexpr int B_ODONE = B_PFULL + 1;
-  static constexpr int B_DRAIN = B_ODONE + 1;
+  static constexpr int B_DRAIN = B_ODONE + 2;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr uint32_t MISC = BAR + 8 * NBAR;
   static constexpr uint32_t BYTES = MISC + 16;
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     mbar_init(bar(L::B_PFULL), 128);
     mbar_init(bar(L::B_ODONE), 1);
+    mbar_init(bar(L::B_ODONE + 1), 1);
     mbar_init(bar(L::B_DRAIN), 1);
     fence_mbar_init();
   }
@@ -192,9 +195,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t va = base + L::V + s * L::TILE;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ts(tbase + kColO, tbase + kColP + 8u * kk, sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024),
-                 idO, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(L::B_ODONE));
+          mma_ts(tbase + kColO, tbase + kColP + 64u * (n & 1) + 8u * kk,
+                 sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024), idO, (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::B_ODONE + (n & 1)));
         mma_commit(bar(L::B_VEMPTY + s));
       }
       // Every MMA issued above completes before TMEM can be released.
@@ -218,14 +221,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int b = n & 1;
       if (!mbar_wait_warp(wc, bar(L::B_SFULL + b), uint32_t(n >> 1) & 1u)) { ok = false; break; }
       tc_fence_after();
+      // All of S at once: four loads in flight, one wait.
       float sv[kTileN];
+      {
+        uint32_t rr[kTileN / 32][32];
 #pragma unroll
-      for (int c = 0; c < kTileN / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + kColS + 128u * b + 32u * c, rr);
-        tmem_ld_wait(rr);
+        for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(lane_addr + kColS + 128u * b + 32u * c, rr[c]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[32 * c + j] = __uint_as_float(rr[j]);
+        for (int c = 0; c < kTileN / 32; ++c) tmem_ld_wait(rr[c]);
+#pragma unroll
+        for (int c = 0; c < kTileN / 32; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sv[32 * c + j] = __uint_as_float(rr[c][j]);
       }
       tc_fence_before();
       mbar_arrive(bar(L::B_SFREE + b));
@@ -236,9 +243,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int j = 0; j < kTileN; ++j)
           if (!(j < ca || (j >= cb && j < ce))) sv[j] = -INFINITY;
       }
-      float mx = sv[0];
+      // Row max as eight independent chains (a single chain would be 127
+      // dependent steps).
+      float mx8[8];
 #pragma unroll
-      for (int j = 1; j < kTileN; ++j) mx = fmaxf(mx, sv[j]);
+      for (int k = 0; k < 8; ++k) mx8[k] = sv[k];
+#pragma unroll
+      for (int j = 8; j < kTileN; j += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], sv[j + k]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_cand = mx * sl2;
       float alpha = 1.f;
       if (m_cand > m_ref + kRescaleThreshold) {
@@ -246,24 +261,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m_ref = m_cand;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P of the previous tile is still read by its PV MMA, and O must be
-      // complete before a rescale: wait for PV(n-1).
-      if (n > 0) {
-        if (!mbar_wait_warp(wc, bar(L::B_ODONE), uint32_t(n - 1) & 1u)) { ok = false; break; }
+      // A rescale needs O complete: wait for P V of tile n-1 (rare once the
+      // running max has settled).
+      if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!mbar_wait_warp(wc, bar(L::B_ODONE + ((n - 1) & 1)), uint32_t((n - 1) >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(lane_addr + kColO + 32u * c, rr);
-            tmem_ld_wait(rr);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(lane_addr + kColO + 32u * c, rr);
+          tmem_ld_wait(rr);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
-            tmem_st32(lane_addr + kColO + 32u * c, rr);
-          }
+          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+          tmem_st32(lane_addr + kColO + 32u * c, rr);
         }
       }
-      float rowsum = 0.f;
+      // P buffer b was last read by P V of tile n-2.
+      if (n >= 2) {
+        if (!mbar_wait_warp(wc, bar(L::B_ODONE + b), uint32_t((n - 2) >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in four chains
 #pragma unroll
       for (int c = 0; c < kTileN / 64; ++c) {
         uint32_t pk[32];
@@ -271,17 +295,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int j = 0; j < 32; ++j) {
           const float p0 = ex2(fmaf(sv[64 * c + 2 * j], sl2, -m_use));
           const float p1 = ex2(fmaf(sv[64 * c + 2 * j + 1], sl2, -m_use));
-          rowsum += p0 + p1;
+          rs[j & 3] += p0 + p1;
           pk[j] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(lane_addr + kColP + 32u * c, pk);
+        tmem_st32(lane_addr + kColP + 64u * b + 32u * c, pk);
       }
-      l = l * alpha + rowsum;
+      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(L::B_PFULL));
     }
-    if (ok && mbar_wait_warp(wc, bar(L::B_ODONE), uint32_t(n_tiles - 1) & 1u)) {
+    if (ok && mbar_wait_warp(wc, bar(L::B_ODONE + ((n_tiles - 1) & 1)),
+                             uint32_t((n_tiles - 1) >> 1) & 1u)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       __nv_bfloat16* orow =
