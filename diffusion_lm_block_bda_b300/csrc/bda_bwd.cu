@@ -21,11 +21,12 @@
 //      and a second warpgroup moves the dQ partial TMEM -> smem, from where
 //      the TMA adds it into the fp32 accumulator (bulk tensor reduce-add).
 //   3. dq_convert: dQ = bf16(scale * accumulator).
-// Roles of the dK/dV kernel (320 threads):
+// Roles of the dK/dV kernel (352 threads):
 //   warps 0..3   softmax: P^T and dS^T, then the dK epilogue
 //   warps 4..7   dQ readout + staging for the TMA reduce, then the dV epilogue
 //   warp 8       producer: K/V once, then Q, dO (TMA) and LSE, D per query tile
 //   warp 9       MMA issuer (one thread)
+//   warp 10      waits on the MMAs' dependencies and gates warp 9
 // TMEM columns: S^T / P^T [0,128) dP^T / dQ [128,256) dK [256,256+D) dV [384,384+D).
 #include <cuda_bf16.h>
 
@@ -100,9 +101,10 @@ __global__ void __launch_bounds__(256) bda_dq_convert_kernel(const float* __rest
 }
 
 // ------------------------------------------------------------------ dK/dV
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 352;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
 constexpr uint32_t kDqBarrier = 1;  // named barrier of the dQ warpgroup (warps 4..7)
+constexpr uint32_t kMmaGate = 2;    // named barrier between the MMA warp and its waiter
 
 // Shared memory (D = 128): K | V | Q x2 | dO | dS^T | dQ staging x2 | LSE x2 |
 // D x2 | barriers = 226.1 KB, so there is no slack to align the base by hand:
@@ -299,93 +301,114 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ndo) drain_wait(wc, bar(L::B_DOFULL), uint32_t(ndo - 1) & 1u);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 9 || warp == 10) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0 && n_iter > 0) {
-      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t idAcc = idesc_bf16(128, D, false, true);    // dV, dK
-      constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ
-      auto issue_s = [&](int i) {  // S_i^T = K Q_i^T
-        const uint32_t qa = base + L::Q + (i & 1) * L::TILE;
+    // Warp 9 issues every MMA (lane 0); warp 10 waits on the mbarriers each
+    // product depends on and opens a named-barrier gate for it.  An mbarrier
+    // wait issued right behind a batch of MMAs queues behind them (hundreds
+    // of cycles even on a completed phase), while a named barrier costs a
+    // few cycles, so the issuing warp only ever meets named barriers.  The
+    // gate also carries the waiter's verdict: a failed wait stops both warps
+    // at the same gate.
+    const bool issuer = warp == 9;
+    auto gate = [&](bool wait_ok) -> bool { return named_bar_and(kMmaGate, 64, wait_ok); };
+    auto wt = [&](int b, uint32_t parity) -> bool { return mbar_wait_warp(wc, bar(b), parity); };
+    constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+    constexpr uint32_t idAcc = idesc_bf16(128, D, false, true);    // dV, dK
+    constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ
+    auto issue_s = [&](int i) {  // S_i^T = K Q_i^T
+      const uint32_t qa = base + L::Q + (i & 1) * L::TILE;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColS, sdesc_sw128(base + L::K + off, 16, 1024),
-                 sdesc_sw128(qa + off, 16, 1024), idSS, kk > 0);
-        }
-        mma_commit(bar(L::B_SFULL));
-      };
-      auto issue_dp = [&]() {  // dP^T = V dO^T
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+        mma_ss(tbase + kColS, sdesc_sw128(base + L::K + off, 16, 1024),
+               sdesc_sw128(qa + off, 16, 1024), idSS, kk > 0);
+      }
+      mma_commit(bar(L::B_SFULL));
+    };
+    auto issue_dp = [&]() {  // dP^T = V dO^T
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColDP, sdesc_sw128(base + L::V + off, 16, 1024),
-                 sdesc_sw128(base + L::DO + off, 16, 1024), idSS, kk > 0);
-        }
-        mma_commit(bar(L::B_DPFULL));
-      };
-      ok = mbar_wait(wc, bar(L::B_KV), 0) && mbar_wait(wc, bar(L::B_QFULL), 0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+        mma_ss(tbase + kColDP, sdesc_sw128(base + L::V + off, 16, 1024),
+               sdesc_sw128(base + L::DO + off, 16, 1024), idSS, kk > 0);
       }
-      ok = ok && mbar_wait(wc, bar(L::B_DOFULL), 0);
-      if (ok) {
+      mma_commit(bar(L::B_DPFULL));
+    };
+    if (n_iter > 0) {
+      bool go = gate(issuer || (wt(L::B_KV, 0) && wt(L::B_QFULL, 0)));
+      if (go && issuer) {
         tc_fence_after();
-        issue_dp();
+        if (lane == 0) issue_s(0);
       }
-      for (int i = 0; ok && i < n_iter; ++i) {
+      go = go && gate(issuer || wt(L::B_DOFULL, 0));
+      if (go && issuer) {
+        tc_fence_after();
+        if (lane == 0) issue_dp();
+      }
+      for (int i = 0; go && i < n_iter; ++i) {
         const uint32_t ph = uint32_t(i) & 1u;
         const int st = i & 1;
         // dV += P^T dO, P^T (bf16 pairs) in the S^T columns
-        if (!mbar_wait(wc, bar(L::B_PFULL), ph)) { ok = false; break; }
-        tc_fence_after();
+        if (!(go = gate(issuer || wt(L::B_PFULL, ph)))) break;
+        if (issuer) {
+          tc_fence_after();
+          if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < kTileM / 16; ++kk)
-          mma_ts(tbase + kColDV, tbase + kColS + 8u * kk,
-                 sdesc_sw128(base + L::DO + 2048u * kk, L::CHUNK, 1024), idAcc,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(L::B_DVDONE));
+            for (int kk = 0; kk < kTileM / 16; ++kk)
+              mma_ts(tbase + kColDV, tbase + kColS + 8u * kk,
+                     sdesc_sw128(base + L::DO + 2048u * kk, L::CHUNK, 1024), idAcc,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(L::B_DVDONE));
+          }
+        }
         // next S^T once its Q is in and dV has read P^T out of the S^T columns
         if (i + 1 < n_iter) {
-          if (!mbar_wait(wc, bar(L::B_QFULL + (st ^ 1)), uint32_t((i + 1) >> 1) & 1u) ||
-              !mbar_wait(wc, bar(L::B_DVDONE), ph)) {
-            ok = false;
+          if (!(go = gate(issuer || (wt(L::B_QFULL + (st ^ 1), uint32_t((i + 1) >> 1) & 1u) &&
+                                     wt(L::B_DVDONE, ph)))))
             break;
+          if (issuer) {
+            tc_fence_after();
+            if (lane == 0) issue_s(i + 1);
           }
-          tc_fence_after();
-          issue_s(i + 1);
         }
         // dQ = dS K, then dK += dS^T Q
-        if (!mbar_wait(wc, bar(L::B_DSFULL), ph)) { ok = false; break; }
-        tc_fence_after();
+        if (!(go = gate(issuer || wt(L::B_DSFULL, ph)))) break;
+        if (issuer) {
+          tc_fence_after();
+          if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ss(tbase + kColDP, sdesc_sw128(base + L::DS + 2048u * kk, L::CHUNK, 1024),
-                 sdesc_sw128(base + L::K + 2048u * kk, L::CHUNK, 1024), idDQ, kk > 0);
-        mma_commit(bar(L::B_DQFULL));
+            for (int kk = 0; kk < kTileN / 16; ++kk)
+              mma_ss(tbase + kColDP, sdesc_sw128(base + L::DS + 2048u * kk, L::CHUNK, 1024),
+                     sdesc_sw128(base + L::K + 2048u * kk, L::CHUNK, 1024), idDQ, kk > 0);
+            mma_commit(bar(L::B_DQFULL));
 #pragma unroll
-        for (int kk = 0; kk < kTileM / 16; ++kk) {
-          const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColDK, sdesc_sw128(base + L::DS + aoff, 16, 1024),
-                 sdesc_sw128(base + L::Q + st * L::TILE + 2048u * kk, L::CHUNK, 1024), idAcc,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kTileM / 16; ++kk) {
+              const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+              mma_ss(tbase + kColDK, sdesc_sw128(base + L::DS + aoff, 16, 1024),
+                     sdesc_sw128(base + L::Q + st * L::TILE + 2048u * kk, L::CHUNK, 1024), idAcc,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(bar(L::B_DSCONS));
+            mma_commit(bar(L::B_QEMPTY + st));
+          }
         }
-        mma_commit(bar(L::B_DSCONS));
-        mma_commit(bar(L::B_QEMPTY + st));
         // next dP^T once dQ has left the dP^T columns and dO_{i+1} is in
         if (i + 1 < n_iter) {
-          if (!mbar_wait(wc, bar(L::B_DQFREE), ph) ||
-              !mbar_wait(wc, bar(L::B_DOFULL), uint32_t(i + 1) & 1u)) {
-            ok = false;
+          if (!(go = gate(issuer || (wt(L::B_DQFREE, ph) &&
+                                     wt(L::B_DOFULL, uint32_t(i + 1) & 1u)))))
             break;
+          if (issuer) {
+            tc_fence_after();
+            if (lane == 0) issue_dp();
           }
-          tc_fence_after();
-          issue_dp();
         }
       }
-      mma_commit(bar(L::B_ACC));
-      drain_wait(wc, bar(L::B_ACC), 0);
+      ok = go;
+      if (issuer && lane == 0) {
+        mma_commit(bar(L::B_ACC));
+        drain_wait(wc, bar(L::B_ACC), 0);
+      }
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------- softmax

@@ -13,6 +13,7 @@
 //   warp 4        TMA producer: Q once, then K and V tiles (NST-stage ring)
 //   warp 5        tcgen05 MMA issuer (one thread): S = Q K^T into TMEM
 //                 (double buffered), O += P V with P read from TMEM
+//   warp 6        waits on the MMAs' dependencies and gates warp 5
 //   warps 0..3    softmax: thread r owns TMEM lane r = query row r; masks
 //                 PARTIAL tiles from block indices, online max/sum, writes P
 //                 as bf16 into TMEM, rescales O when the max grows by more
@@ -30,7 +31,8 @@ namespace bda {
 
 namespace {
 
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 224;
+constexpr uint32_t kMmaGate = 1;  // named barrier between the MMA warp and its waiter
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // P0 at kColP, P1 at kColP + 64
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
 
@@ -163,48 +165,74 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 5 || warp == 6) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
-      bool ok = mbar_wait(wc, bar(L::B_QFULL), 0);
-      auto issue_s = [&](int n) -> bool {
-        const int s = n % NST, b = n & 1;
-        if (!mbar_wait(wc, bar(L::B_KFULL + s), uint32_t(n / NST) & 1u)) return false;
-        if (n >= 2 && !mbar_wait(wc, bar(L::B_SFREE + b), uint32_t((n >> 1) - 1) & 1u)) return false;
-        tc_fence_after();
-        const uint32_t qa = base + L::Q, ka = base + L::K + s * L::TILE;
+    // Warp 5 issues every MMA (lane 0); warp 6 waits on the mbarriers each
+    // product depends on and opens a named-barrier gate for it.  An mbarrier
+    // wait issued right behind a batch of MMAs queues behind them (hundreds
+    // of cycles even on a completed phase), while a named barrier costs a
+    // few cycles, so the issuing warp only ever meets named barriers.  The
+    // gate also carries the waiter's verdict: a failed wait stops both warps
+    // at the same gate.
+    const bool issuer = warp == 5;
+    auto gate = [&](bool wait_ok) -> bool { return named_bar_and(kMmaGate, 64, wait_ok); };
+    auto wt = [&](int b, uint32_t parity) -> bool { return mbar_wait_warp(wc, bar(b), parity); };
+    constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+    // S(n) waits for K(n) and for the softmax to have read S(n-2) out of its buffer.
+    auto s_ready = [&](int n) -> bool {
+      const int s = n % NST, b = n & 1;
+      return wt(L::B_KFULL + s, uint32_t(n / NST) & 1u) &&
+             (n < 2 || wt(L::B_SFREE + b, uint32_t((n >> 1) - 1) & 1u));
+    };
+    auto issue_s = [&](int n) {
+      const int s = n % NST, b = n & 1;
+      const uint32_t qa = base + L::Q, ka = base + L::K + s * L::TILE;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColS + 128u * b, sdesc_sw128(qa + off, 16, 1024),
-                 sdesc_sw128(ka + off, 16, 1024), idS, kk > 0);
-        }
-        mma_commit(bar(L::B_SFULL + b));
-        mma_commit(bar(L::B_KEMPTY + s));
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int n = 0; ok && n < n_tiles; ++n) {
-        if (n + 1 < n_tiles && !issue_s(n + 1)) { ok = false; break; }
-        const int s = n % NST;
-        if (!mbar_wait(wc, bar(L::B_PFULL), uint32_t(n) & 1u)) { ok = false; break; }
-        if (!mbar_wait(wc, bar(L::B_VFULL + s), uint32_t(n / NST) & 1u)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t va = base + L::V + s * L::TILE;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ts(tbase + kColO, tbase + kColP + 64u * (n & 1) + 8u * kk,
-                 sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024), idO, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(L::B_ODONE + (n & 1)));
-        mma_commit(bar(L::B_VEMPTY + s));
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+        mma_ss(tbase + kColS + 128u * b, sdesc_sw128(qa + off, 16, 1024),
+               sdesc_sw128(ka + off, 16, 1024), idS, kk > 0);
       }
+      mma_commit(bar(L::B_SFULL + b));
+      mma_commit(bar(L::B_KEMPTY + s));
+    };
+    bool go = gate(issuer || (wt(L::B_QFULL, 0) && s_ready(0)));
+    if (go && issuer) {
+      tc_fence_after();
+      if (lane == 0) issue_s(0);
+    }
+    for (int n = 0; go && n < n_tiles; ++n) {
+      if (n + 1 < n_tiles) {
+        if (!(go = gate(issuer || s_ready(n + 1)))) break;
+        if (issuer) {
+          tc_fence_after();
+          if (lane == 0) issue_s(n + 1);
+        }
+      }
+      const int s = n % NST;
+      if (!(go = gate(issuer || (wt(L::B_PFULL, uint32_t(n) & 1u) &&
+                                 wt(L::B_VFULL + s, uint32_t(n / NST) & 1u)))))
+        break;
+      if (issuer) {
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t va = base + L::V + s * L::TILE;
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ts(tbase + kColO, tbase + kColP + 64u * (n & 1) + 8u * kk,
+                   sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024), idO, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(L::B_ODONE + (n & 1)));
+          mma_commit(bar(L::B_VEMPTY + s));
+        }
+      }
+    }
+    if (issuer && lane == 0) {
       // Every MMA issued above completes before TMEM can be released.
       mma_commit(bar(L::B_DRAIN));
       drain_wait(wc, bar(L::B_DRAIN), 0);
     }
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------------------- softmax
     const int r = tid;  // TMEM lane == query row of the tile
     const int t_local = r >> a.lg_hg;
