@@ -162,14 +162,31 @@ def measured_peaks():
     return 1800.0, 1400.0, 6400.0, "fallback"
 
 
+KERNEL_SOURCES = ("diffusion_lm_block_bda_b300/csrc/bda_bwd.cu", "diffusion_lm_block_bda_b300/csrc/bda_ptx.cuh",
+                  "diffusion_lm_block_bda_b300/csrc/bda_internal.h",
+                  "diffusion_lm_block_bda_b300/csrc/bda_kernels.h")
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic():
-    """dram bytes per launch of the backward dK/dV kernel from the committed ncu
-    summary (None when absent or taken on an older kernel build)."""
+    """DRAM bytes per launch of the backward dK/dV kernel from the committed ncu
+    summary; None when absent or taken on a different build of the kernel
+    (the summary records a hash of the kernel's sources)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         j = json.load(f)
+    if j.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
     return j.get("bwd_dkdv_bytes_per_launch")
 
 
