@@ -66,9 +66,11 @@ __device__ __forceinline__ void raise_abort(WaitCtx w, uint32_t code) {
 
 // Wait for the completion of the phase with the given parity.  Returns false
 // (and leaves the CTA in abort state) if the CTA is aborting or the limit
-// passes.
-static __device__ __noinline__ bool mbar_wait(WaitCtx w, uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// passes.  The first poll is inlined at every call site; only a wait that
+// does not succeed at once enters the out-of-line loop (a call at every site
+// measured slower in the kernels, and a fully inlined loop slower still in
+// the backward, whose many wait sites it bloats).
+static __device__ __noinline__ bool mbar_wait_slow(WaitCtx w, uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -80,6 +82,11 @@ static __device__ __noinline__ bool mbar_wait(WaitCtx w, uint32_t bar, uint32_t 
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(WaitCtx w, uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(w, bar, parity);
 }
 
 // Warp-collective variant: every lane waits, the outcome is warp-uniform.
