@@ -7,10 +7,14 @@
 // shared memory and an online softmax keeps a running max and sum, so the
 // L x L score matrix never exists.
 //
-// One CTA per (query tile, group of hg query heads); the tile is tok = 128/hg
-// tokens x hg heads of one KV group, so the KV heads' K/V tile feeds all 128
-// rows (GQA packing).  Roles:
-//   warp 4        TMA producer: Q once, then K and V tiles (NST-stage ring)
+// A work unit is (query tile, group of hg query heads); the tile is tok =
+// 128/hg tokens x hg heads of one KV group, so the KV head's K/V tile feeds
+// all 128 rows (GQA packing).  The kernel is persistent: one CTA per SM walks
+// its share of the units (the planner's longest-first list, dealt out in
+// snake order), and every pipeline (Q buffers, the K/V ring, S and P buffers)
+// runs on across unit boundaries, so the next unit's loads and first S
+// product overlap the current unit's last softmax and epilogue.  Roles:
+//   warp 4        TMA producer: Q (two buffers), then K and V tiles (NST-stage ring)
 //   warp 5        tcgen05 MMA issuer (one thread): S = Q K^T into TMEM
 //                 (double buffered), O += P V with P read from TMEM
 //   warp 6        waits on the MMAs' dependencies and gates warp 5
@@ -41,14 +45,15 @@ struct FwdLayout {
   static constexpr int CH = D / 64;              // 128-byte chunks of a head_dim row
   static constexpr uint32_t CHUNK = 128 * 128;   // one [128 rows][64 bf16] swizzled chunk
   static constexpr uint32_t TILE = CH * CHUNK;
-  static constexpr uint32_t Q = 0;
-  static constexpr uint32_t K = Q + TILE;
+  static constexpr uint32_t Q = 0;               // two buffers
+  static constexpr uint32_t K = Q + 2 * TILE;
   static constexpr uint32_t V = K + NST * TILE;
   static constexpr uint32_t BAR = V + NST * TILE;
-  // q_full, k_full[NST], k_empty[NST], v_full[NST], v_empty[NST],
-  // s_full[2], s_free[2], p_full, o_done[2] (per P buffer), drain
+  // q_full[2], q_empty[2], k_full[NST], k_empty[NST], v_full[NST], v_empty[NST],
+  // s_full[2], s_free[2], p_full, o_done[2] (per P buffer), o_free, drain
   static constexpr int B_QFULL = 0;
-  static constexpr int B_KFULL = 1;
+  static constexpr int B_QEMPTY = 2;
+  static constexpr int B_KFULL = 4;
   static constexpr int B_KEMPTY = B_KFULL + NST;
   static constexpr int B_VFULL = B_KEMPTY + NST;
   static constexpr int B_VEMPTY = B_VFULL + NST;
@@ -56,7 +61,8 @@ struct FwdLayout {
   static constexpr int B_SFREE = B_SFULL + 2;
   static constexpr int B_PFULL = B_SFREE + 2;
   static constexpr int B_ODONE = B_PFULL + 1;
-  static constexpr int B_DRAIN = B_ODONE + 2;
+  static constexpr int B_OFREE = B_ODONE + 2;
+  static constexpr int B_DRAIN = B_OFREE + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr uint32_t MISC = BAR + 8 * NBAR;
   static constexpr uint32_t BYTES = MISC + 16;
@@ -76,6 +82,15 @@ __device__ __forceinline__ bool drain_wait(WaitCtx w, uint32_t bar, uint32_t par
   return true;
 }
 
+// The k-th unit (k = 0, 1, ...) of this CTA: units are dealt to the CTAs in
+// snake order over the longest-first list (forward in even rounds, backward
+// in odd ones), which evens out the CTAs' totals.  -1 past the end.
+__device__ __forceinline__ int unit_of(int k, int n_units) {
+  const int g = int(gridDim.x), c = int(blockIdx.x);
+  const int u = k * g + ((k & 1) ? g - 1 - c : c);
+  return u < n_units ? u : -1;
+}
+
 template <int D, int NST>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     bda_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -89,18 +104,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   auto bar = [&](int i) -> uint32_t { return base + L::BAR + 8u * uint32_t(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::MISC + 4);
-
-  const int item_idx = blockIdx.x / a.n_groups;
-  const int grp = blockIdx.x - item_idx * a.n_groups;
-  const FwdItem it = a.items[item_idx];
-  const int head0 = grp * a.hg;
-  const int kvh = head0 / a.G;
-  const int n_tiles = it.r1_end + (it.r2_end - it.r2_begin);
-  auto key_tile = [&](int n) -> int { return n < it.r1_end ? n : it.r2_begin + (n - it.r1_end); };
+  const int n_units = a.n_units;
 
   if (tid == 0) {
     *abort_flag = 0;
-    mbar_init(bar(L::B_QFULL), 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(bar(L::B_QFULL + q), 1);
+      mbar_init(bar(L::B_QEMPTY + q), 1);
+    }
     for (int s = 0; s < NST; ++s) {
       mbar_init(bar(L::B_KFULL + s), 1);
       mbar_init(bar(L::B_KEMPTY + s), 1);
@@ -110,10 +121,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::B_SFULL + b), 1);
       mbar_init(bar(L::B_SFREE + b), 128);
+      mbar_init(bar(L::B_ODONE + b), 1);
     }
     mbar_init(bar(L::B_PFULL), 128);
-    mbar_init(bar(L::B_ODONE), 1);
-    mbar_init(bar(L::B_ODONE + 1), 1);
+    mbar_init(bar(L::B_OFREE), 128);
     mbar_init(bar(L::B_DRAIN), 1);
     fence_mbar_init();
   }
@@ -127,38 +138,69 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tbase = *tmem_slot;
   const WaitCtx wc{abort_flag, a.status, a.timeout_ns};
 
+  // Unit u: work item, head group, and its key tiles.
+  struct Unit {
+    FwdItem it;
+    int head0, kvh, n_tiles;
+  };
+  auto load_unit = [&](int u) -> Unit {
+    Unit x;
+    const int item_idx = u / a.n_groups;
+    const int grp = u - item_idx * a.n_groups;
+    x.it = a.items[item_idx];
+    x.head0 = grp * a.hg;
+    x.kvh = x.head0 / a.G;
+    x.n_tiles = x.it.r1_end + (x.it.r2_end - x.it.r2_begin);
+    return x;
+  };
+  auto key_tile = [](const FwdItem& it, int n) -> int {
+    return n < it.r1_end ? n : it.r2_begin + (n - it.r1_end);
+  };
+
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int nk[NST], nv[NST];
+      int nq[2] = {0, 0}, nk[NST], nv[NST];  // copies issued per barrier (abort drain)
       for (int s = 0; s < NST; ++s) nk[s] = nv[s] = 0;
-      mbar_arrive_expect_tx(bar(L::B_QFULL), L::TILE);
-      for (int c = 0; c < L::CH; ++c)
-        tma_load_3d(base + L::Q + c * L::CHUNK, &tm_q, bar(L::B_QFULL), c * 64, head0, it.q_row);
       bool ok = true;
-      for (int n = 0; n < n_tiles && ok; ++n) {
-        const int s = n % NST;
-        const uint32_t ph = uint32_t(n / NST) & 1u;
-        const int krow = it.k_row + key_tile(n) * kTileN;
-        if (n >= NST && !mbar_wait(wc, bar(L::B_KEMPTY + s), ph ^ 1u)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(L::B_KFULL + s), L::TILE);
+      int g = 0;  // key tiles streamed so far (all units)
+      for (int k = 0, u; ok && (u = unit_of(k, n_units)) >= 0; ++k) {
+        const Unit x = load_unit(u);
+        const int qb = k & 1;
+        if (k >= 2 && !mbar_wait(wc, bar(L::B_QEMPTY + qb), uint32_t((k >> 1) - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(L::B_QFULL + qb), L::TILE);
         for (int c = 0; c < L::CH; ++c)
-          tma_load_3d(base + L::K + s * L::TILE + c * L::CHUNK, &tm_k, bar(L::B_KFULL + s), c * 64,
-                      kvh, krow);
-        ++nk[s];
-        if (n >= NST && !mbar_wait(wc, bar(L::B_VEMPTY + s), ph ^ 1u)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::TILE);
-        for (int c = 0; c < L::CH; ++c)
-          tma_load_3d(base + L::V + s * L::TILE + c * L::CHUNK, &tm_v, bar(L::B_VFULL + s), c * 64,
-                      kvh, krow);
-        ++nv[s];
+          tma_load_3d(base + L::Q + qb * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + qb),
+                      c * 64, x.head0, x.it.q_row);
+        ++nq[qb];
+        for (int n = 0; n < x.n_tiles; ++n, ++g) {
+          const int s = g % NST;
+          const uint32_t ph = uint32_t(g / NST) & 1u;
+          const int krow = x.it.k_row + key_tile(x.it, n) * kTileN;
+          if (g >= NST && !mbar_wait(wc, bar(L::B_KEMPTY + s), ph ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(L::B_KFULL + s), L::TILE);
+          for (int c = 0; c < L::CH; ++c)
+            tma_load_3d(base + L::K + s * L::TILE + c * L::CHUNK, &tm_k, bar(L::B_KFULL + s),
+                        c * 64, x.kvh, krow);
+          ++nk[s];
+          if (g >= NST && !mbar_wait(wc, bar(L::B_VEMPTY + s), ph ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::TILE);
+          for (int c = 0; c < L::CH; ++c)
+            tma_load_3d(base + L::V + s * L::TILE + c * L::CHUNK, &tm_v, bar(L::B_VFULL + s),
+                        c * 64, x.kvh, krow);
+          ++nv[s];
+        }
       }
       if (!ok || *abort_flag) {
         // Let every copy already issued land before the CTA can exit.
-        drain_wait(wc, bar(L::B_QFULL), 0);
+        for (int q = 0; q < 2; ++q)
+          if (nq[q]) drain_wait(wc, bar(L::B_QFULL + q), uint32_t(nq[q] - 1) & 1u);
         for (int s = 0; s < NST; ++s) {
           if (nk[s]) drain_wait(wc, bar(L::B_KFULL + s), uint32_t(nk[s] - 1) & 1u);
           if (nv[s]) drain_wait(wc, bar(L::B_VFULL + s), uint32_t(nv[s] - 1) & 1u);
@@ -179,15 +221,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     auto wt = [&](int b, uint32_t parity) -> bool { return mbar_wait_warp(wc, bar(b), parity); };
     constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
     constexpr uint32_t idO = idesc_bf16(128, D, false, true);
-    // S(n) waits for K(n) and for the softmax to have read S(n-2) out of its buffer.
-    auto s_ready = [&](int n) -> bool {
-      const int s = n % NST, b = n & 1;
-      return wt(L::B_KFULL + s, uint32_t(n / NST) & 1u) &&
-             (n < 2 || wt(L::B_SFREE + b, uint32_t((n >> 1) - 1) & 1u));
+    // S(g) waits for K(g) and for the softmax to have read S(g-2) out of its buffer.
+    auto s_ready = [&](int g) -> bool {
+      const int s = g % NST, b = g & 1;
+      return wt(L::B_KFULL + s, uint32_t(g / NST) & 1u) &&
+             (g < 2 || wt(L::B_SFREE + b, uint32_t((g >> 1) - 1) & 1u));
     };
-    auto issue_s = [&](int n) {
-      const int s = n % NST, b = n & 1;
-      const uint32_t qa = base + L::Q, ka = base + L::K + s * L::TILE;
+    auto issue_s = [&](int g, int qb, bool last_of_unit) {
+      const int s = g % NST, b = g & 1;
+      const uint32_t qa = base + L::Q + qb * L::TILE, ka = base + L::K + s * L::TILE;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
@@ -196,34 +238,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       mma_commit(bar(L::B_SFULL + b));
       mma_commit(bar(L::B_KEMPTY + s));
+      if (last_of_unit) mma_commit(bar(L::B_QEMPTY + qb));
     };
-    bool go = gate(issuer || (wt(L::B_QFULL, 0) && s_ready(0)));
-    if (go && issuer) {
-      tc_fence_after();
-      if (lane == 0) issue_s(0);
-    }
-    for (int n = 0; go && n < n_tiles; ++n) {
-      if (n + 1 < n_tiles) {
-        if (!(go = gate(issuer || s_ready(n + 1)))) break;
-        if (issuer) {
-          tc_fence_after();
-          if (lane == 0) issue_s(n + 1);
-        }
-      }
-      const int s = n % NST;
-      if (!(go = gate(issuer || (wt(L::B_PFULL, uint32_t(n) & 1u) &&
-                                 wt(L::B_VFULL + s, uint32_t(n / NST) & 1u)))))
+    bool go = true;
+    int g = 0;  // key tiles issued so far (all units)
+    for (int k = 0, u; go && (u = unit_of(k, n_units)) >= 0; ++k) {
+      const Unit x = load_unit(u);
+      const int qb = k & 1;
+      if (!(go = gate(issuer || (wt(L::B_QFULL + qb, uint32_t(k >> 1) & 1u) && s_ready(g)))))
         break;
       if (issuer) {
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t va = base + L::V + s * L::TILE;
+        if (lane == 0) issue_s(g, qb, x.n_tiles == 1);
+      }
+      for (int n = 0; n < x.n_tiles; ++n, ++g) {
+        if (n + 1 < x.n_tiles) {
+          if (!(go = gate(issuer || s_ready(g + 1)))) break;
+          if (issuer) {
+            tc_fence_after();
+            if (lane == 0) issue_s(g + 1, qb, n + 2 == x.n_tiles);
+          }
+        }
+        // O += P V; the unit's first product overwrites O, so the previous
+        // unit's epilogue must have read it out.
+        const int s = g % NST;
+        if (!(go = gate(issuer || (wt(L::B_PFULL, uint32_t(g) & 1u) &&
+                                   wt(L::B_VFULL + s, uint32_t(g / NST) & 1u) &&
+                                   (n > 0 || k == 0 || wt(L::B_OFREE, uint32_t(k - 1) & 1u))))))
+          break;
+        if (issuer) {
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t va = base + L::V + s * L::TILE;
 #pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk)
-            mma_ts(tbase + kColO, tbase + kColP + 64u * (n & 1) + 8u * kk,
-                   sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024), idO, (n > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(L::B_ODONE + (n & 1)));
-          mma_commit(bar(L::B_VEMPTY + s));
+            for (int kk = 0; kk < kTileN / 16; ++kk)
+              mma_ts(tbase + kColO, tbase + kColP + 64u * (g & 1) + 8u * kk,
+                     sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024), idO, (n > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(L::B_ODONE + (g & 1)));
+            mma_commit(bar(L::B_VEMPTY + s));
+          }
         }
       }
     }
@@ -237,128 +290,141 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int r = tid;  // TMEM lane == query row of the tile
     const int t_local = r >> a.lg_hg;
     const int hh = r & (a.hg - 1);
-    const bool row_valid = t_local < it.q_len;
-    const int p = it.pos0 + (row_valid ? t_local : it.q_len - 1);
-    const RowKeys rk = row_keys(p, it.prefix, a.block, it.lk);
     const uint32_t lane_addr = tbase + (uint32_t(warp * 32) << 16);
     const float sl2 = a.scale_log2;
-    float m_ref = -INFINITY;  // running max of scale*log2(e)*S, the reference of P
-    float l = 0.f;            // running sum of P (relative to m_ref)
     bool ok = true;
-    for (int n = 0; n < n_tiles; ++n) {
-      const int b = n & 1;
-      if (!mbar_wait_warp(wc, bar(L::B_SFULL + b), uint32_t(n >> 1) & 1u)) { ok = false; break; }
-      tc_fence_after();
-      // All of S at once: four loads in flight, one wait.
-      float sv[kTileN];
-      {
-        uint32_t rr[kTileN / 32][32];
-#pragma unroll
-        for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(lane_addr + kColS + 128u * b + 32u * c, rr[c]);
-#pragma unroll
-        for (int c = 0; c < kTileN / 32; ++c) tmem_ld_wait(rr[c]);
-#pragma unroll
-        for (int c = 0; c < kTileN / 32; ++c)
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sv[32 * c + j] = __uint_as_float(rr[c][j]);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(L::B_SFREE + b));
-      if (n >= it.n_full) {  // PARTIAL tile: mask from block indices
-        const int k0 = key_tile(n) * kTileN;
-        const int ca = rk.a - k0, cb = rk.b - k0, ce = rk.e - k0;
-#pragma unroll
-        for (int j = 0; j < kTileN; ++j)
-          if (!(j < ca || (j >= cb && j < ce))) sv[j] = -INFINITY;
-      }
-      // Row max as eight independent chains (a single chain would be 127
-      // dependent steps).
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = sv[k];
-#pragma unroll
-      for (int j = 8; j < kTileN; j += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], sv[j + k]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_cand = mx * sl2;
-      float alpha = 1.f;
-      if (m_cand > m_ref + kRescaleThreshold) {
-        alpha = ex2(m_ref - m_cand);  // 0 on the first finite max
-        m_ref = m_cand;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // A rescale needs O complete: wait for P V of tile n-1 (rare once the
-      // running max has settled).
-      if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!mbar_wait_warp(wc, bar(L::B_ODONE + ((n - 1) & 1)), uint32_t((n - 1) >> 1) & 1u)) {
-          ok = false;
-          break;
-        }
+    int g = 0;  // key tiles consumed so far (all units)
+    for (int k = 0, u; ok && (u = unit_of(k, n_units)) >= 0; ++k) {
+      const Unit x = load_unit(u);
+      const FwdItem& it = x.it;
+      const bool row_valid = t_local < it.q_len;
+      const int p = it.pos0 + (row_valid ? t_local : it.q_len - 1);
+      const RowKeys rk = row_keys(p, it.prefix, a.block, it.lk);
+      float m_ref = -INFINITY;  // running max of scale*log2(e)*S, the reference of P
+      float l = 0.f;            // running sum of P (relative to m_ref)
+      for (int n = 0; n < x.n_tiles; ++n, ++g) {
+        const int b = g & 1;
+        if (!mbar_wait_warp(wc, bar(L::B_SFULL + b), uint32_t(g >> 1) & 1u)) { ok = false; break; }
         tc_fence_after();
+        // All of S at once: four loads in flight, one wait.
+        float sv[kTileN];
+        {
+          uint32_t rr[kTileN / 32][32];
+#pragma unroll
+          for (int c = 0; c < kTileN / 32; ++c)
+            tmem_ld32(lane_addr + kColS + 128u * b + 32u * c, rr[c]);
+#pragma unroll
+          for (int c = 0; c < kTileN / 32; ++c) tmem_ld_wait(rr[c]);
+#pragma unroll
+          for (int c = 0; c < kTileN / 32; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sv[32 * c + j] = __uint_as_float(rr[c][j]);
+        }
+        tc_fence_before();
+        mbar_arrive(bar(L::B_SFREE + b));
+        if (n >= it.n_full) {  // PARTIAL tile: mask from block indices
+          const int k0 = key_tile(it, n) * kTileN;
+          const int ca = rk.a - k0, cb = rk.b - k0, ce = rk.e - k0;
+#pragma unroll
+          for (int j = 0; j < kTileN; ++j)
+            if (!(j < ca || (j >= cb && j < ce))) sv[j] = -INFINITY;
+        }
+        // Row max as eight independent chains (a single chain would be 127
+        // dependent steps).
+        float mx8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx8[q] = sv[q];
+#pragma unroll
+        for (int j = 8; j < kTileN; j += 8)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx8[q] = fmaxf(mx8[q], sv[j + q]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float m_cand = mx * sl2;
+        float alpha = 1.f;
+        if (m_cand > m_ref + kRescaleThreshold) {
+          alpha = ex2(m_ref - m_cand);  // 0 on the first finite max
+          m_ref = m_cand;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // A rescale needs O complete: wait for P V of the previous tile (rare
+        // once the running max has settled).
+        if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!mbar_wait_warp(wc, bar(L::B_ODONE + ((g - 1) & 1)), uint32_t((g - 1) >> 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(lane_addr + kColO + 32u * c, rr);
+            tmem_ld_wait(rr);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+            tmem_st32(lane_addr + kColO + 32u * c, rr);
+          }
+        }
+        // P buffer b was last read by P V of tile g-2.
+        if (g >= 2) {
+          if (!mbar_wait_warp(wc, bar(L::B_ODONE + b), uint32_t((g - 2) >> 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in four chains
+#pragma unroll
+        for (int c = 0; c < kTileN / 64; ++c) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float p0 = ex2(fmaf(sv[64 * c + 2 * j], sl2, -m_use));
+            const float p1 = ex2(fmaf(sv[64 * c + 2 * j + 1], sl2, -m_use));
+            rs[j & 3] += p0 + p1;
+            pk[j] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(lane_addr + kColP + 64u * b + 32u * c, pk);
+        }
+        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(L::B_PFULL));
+      }
+      if (!ok) break;
+      // Epilogue: O out of TMEM (then the next unit's first P V may
+      // overwrite it), O / l and LSE to global memory.
+      const int gl = g - 1;  // the unit's last key tile
+      if (!mbar_wait_warp(wc, bar(L::B_ODONE + (gl & 1)), uint32_t(gl >> 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t ov[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_addr + kColO + 32u * c, ov[c]);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld_wait(ov[c]);
+      tc_fence_before();
+      mbar_arrive(bar(L::B_OFREE));
+      if (row_valid) {
+        const float inv_l = 1.f / l;
+        __nv_bfloat16* orow =
+            a.o + (size_t(it.q_row + t_local) * a.hq + size_t(x.head0 + hh)) * size_t(D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(lane_addr + kColO + 32u * c, rr);
-          tmem_ld_wait(rr);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
-          tmem_st32(lane_addr + kColO + 32u * c, rr);
-        }
-      }
-      // P buffer b was last read by P V of tile n-2.
-      if (n >= 2) {
-        if (!mbar_wait_warp(wc, bar(L::B_ODONE + b), uint32_t((n - 2) >> 1) & 1u)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in four chains
-#pragma unroll
-      for (int c = 0; c < kTileN / 64; ++c) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float p0 = ex2(fmaf(sv[64 * c + 2 * j], sl2, -m_use));
-          const float p1 = ex2(fmaf(sv[64 * c + 2 * j + 1], sl2, -m_use));
-          rs[j & 3] += p0 + p1;
-          pk[j] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(lane_addr + kColP + 64u * b + 32u * c, pk);
-      }
-      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(L::B_PFULL));
-    }
-    if (ok && mbar_wait_warp(wc, bar(L::B_ODONE + ((n_tiles - 1) & 1)),
-                             uint32_t((n_tiles - 1) >> 1) & 1u)) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      __nv_bfloat16* orow =
-          a.o + (size_t(it.q_row + t_local) * a.hq + size_t(head0 + hh)) * size_t(D);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + kColO + 32u * c, rr);
-        tmem_ld_wait(rr);
-        if (row_valid) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(__uint_as_float(rr[2 * j]) * inv_l,
-                                __uint_as_float(rr[2 * j + 1]) * inv_l);
+            pk[j] = pack_bf16x2(__uint_as_float(ov[c][2 * j]) * inv_l,
+                                __uint_as_float(ov[c][2 * j + 1]) * inv_l);
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
-      }
-      if (row_valid) {
         const float lse2 = m_ref + log2f(l);
-        a.lse[size_t(head0 + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
+        a.lse[size_t(x.head0 + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
             lse2 * 0.69314718055994530942f;
       }
     }
@@ -372,15 +438,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
+int fwd_sm_count() {
+  static int n = [] {
+    int dev = 0, v = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      return v;
+    return 148;
+  }();
+  return n;
+}
+
 template <int D, int NST>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdArgs& a, int n_items, cudaStream_t stream) {
   using L = FwdLayout<D, NST>;
+  static_assert(L::ALLOC <= 232448, "forward shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(bda_fwd_kernel<D, NST>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::ALLOC));
   if (e != cudaSuccess) return e;
-  const unsigned grid = unsigned(n_items) * unsigned(a.n_groups);
-  bda_fwd_kernel<D, NST><<<grid, kFwdThreads, L::ALLOC, stream>>>(tq, tk, tv, a);
+  FwdArgs args = a;
+  args.n_units = n_items * a.n_groups;
+  const int grid = args.n_units < fwd_sm_count() ? args.n_units : fwd_sm_count();
+  bda_fwd_kernel<D, NST><<<unsigned(grid), kFwdThreads, L::ALLOC, stream>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }
 

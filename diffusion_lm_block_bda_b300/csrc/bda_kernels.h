@@ -16,7 +16,8 @@ struct FwdArgs {
   float* lse;
   uint32_t* status;
   uint64_t timeout_ns;
-  int n_groups;  // hq / hg: CTAs per work item
+  int n_groups;  // hq / hg: head groups per work item (a unit = item x group)
+  int n_units;   // items x n_groups; set by launch_fwd
   int hg, lg_hg;
   int G;         // hq / hkv
   int hq;
