@@ -499,12 +499,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t pk[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint32_t pb = pp[16 * c + 4 * u4 + j];
+            // dP - D in fp32, rounded to a bf16 pair, times the bf16 pair of
+            // P in one packed multiply (dS is stored as bf16 anyway).
             const int cc = 8 * u4 + 2 * j;
-            const float v0 = __uint_as_float(pb << 16) * (__uint_as_float(r[cc]) - dd[2 * j]);
-            const float v1 = __uint_as_float(pb & 0xffff0000u) *
-                             (__uint_as_float(r[cc + 1]) - dd[2 * j + 1]);
-            pk[j] = pack_bf16x2(v0, v1);
+            pk[j] = mul_bf16x2(pp[16 * c + 4 * u4 + j],
+                               pack_bf16x2(__uint_as_float(r[cc]) - dd[2 * j],
+                                           __uint_as_float(r[cc + 1]) - dd[2 * j + 1]));
           }
           const int u = 4 * c + u4;
           *reinterpret_cast<uint4*>(dsb + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =

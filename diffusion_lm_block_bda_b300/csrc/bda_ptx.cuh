@@ -310,6 +310,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Element-wise product of two bf16 pairs, rounded to nearest even.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Byte offset of the 16-byte unit `u` (0..7) of row `r` inside a 128-byte
 // swizzled [rows][128 B] tile whose base is 1024-byte aligned.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t u) {
