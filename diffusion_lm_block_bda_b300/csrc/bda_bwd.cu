@@ -313,6 +313,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool issuer = warp == 9;
     auto gate = [&](bool wait_ok) -> bool { return named_bar_and(kMmaGate, 64, wait_ok); };
     auto wt = [&](int b, uint32_t parity) -> bool { return mbar_wait_warp(wc, bar(b), parity); };
+    auto wt2 = [&](int b1, uint32_t p1, int b2, uint32_t p2) -> bool {
+      return mbar_wait2_warp(wc, bar(b1), p1, bar(b2), p2);
+    };
     constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
     constexpr uint32_t idAcc = idesc_bf16(128, D, false, true);    // dV, dK
     constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(bar(L::B_DPFULL));
     };
     if (n_iter > 0) {
-      bool go = gate(issuer || (wt(L::B_KV, 0) && wt(L::B_QFULL, 0)));
+      bool go = gate(issuer || wt2(L::B_KV, 0, L::B_QFULL, 0));
       if (go && issuer) {
         tc_fence_after();
         if (lane == 0) issue_s(0);
@@ -364,8 +367,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         // next S^T once its Q is in and dV has read P^T out of the S^T columns
         if (i + 1 < n_iter) {
-          if (!(go = gate(issuer || (wt(L::B_QFULL + (st ^ 1), uint32_t((i + 1) >> 1) & 1u) &&
-                                     wt(L::B_DVDONE, ph)))))
+          if (!(go = gate(issuer || wt2(L::B_QFULL + (st ^ 1), uint32_t((i + 1) >> 1) & 1u,
+                                        L::B_DVDONE, ph))))
             break;
           if (issuer) {
             tc_fence_after();
@@ -395,8 +398,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         // next dP^T once dQ has left the dP^T columns and dO_{i+1} is in
         if (i + 1 < n_iter) {
-          if (!(go = gate(issuer || (wt(L::B_DQFREE, ph) &&
-                                     wt(L::B_DOFULL, uint32_t(i + 1) & 1u)))))
+          if (!(go = gate(issuer || wt2(L::B_DOFULL, uint32_t(i + 1) & 1u, L::B_DQFREE, ph))))
             break;
           if (issuer) {
             tc_fence_after();
@@ -433,8 +435,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int c_hi = hi_c <= lo_c ? c_lo : min(hi_c, a.tok) << a.lg_hg;
       const bool warp_full = __all_sync(0xffffffffu, c_lo == 0 && c_hi >= kTileM);
       // QFULL publishes the producer's LSE / D staging to these threads.
-      if (!mbar_wait_warp(wc, bar(L::B_QFULL + st), uint32_t(i >> 1) & 1u)) { ok = false; break; }
-      if (!mbar_wait_warp(wc, bar(L::B_SFULL), ph)) { ok = false; break; }
+      if (!mbar_wait2_warp(wc, bar(L::B_QFULL + st), uint32_t(i >> 1) & 1u, bar(L::B_SFULL), ph)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       // P^T = exp(scale S^T - LSE), masked, 32 query columns at a time; the
       // bf16 pairs go back into the S^T columns already read (chunk c fills
@@ -486,10 +490,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(L::B_PFULL));
-      // dS^T = P^T o (dP^T - D) -> bf16 smem (K-major for dK, read MN-major for dQ)
-      if (!mbar_wait_warp(wc, bar(L::B_DPFULL), ph)) { ok = false; break; }
+      // dS^T = P^T o (dP^T - D) -> bf16 smem (K-major for dK, read MN-major for dQ);
       // the dS^T buffer is free once dQ and dK of the previous tile ran
-      if (i > 0 && !mbar_wait_warp(wc, bar(L::B_DSCONS), uint32_t(i - 1) & 1u)) { ok = false; break; }
+      const bool dp_ok = i == 0 ? mbar_wait_warp(wc, bar(L::B_DPFULL), ph)
+                                : mbar_wait2_warp(wc, bar(L::B_DSCONS), uint32_t(i - 1) & 1u,
+                                                  bar(L::B_DPFULL), ph);
+      if (!dp_ok) { ok = false; break; }
       tc_fence_after();
       auto ds_chunk = [&](int c, const uint32_t (&r)[32]) {
 #pragma unroll

@@ -14,7 +14,8 @@
 // snake order), and every pipeline (Q buffers, the K/V ring, S and P buffers)
 // runs on across unit boundaries, so the next unit's loads and first S
 // product overlap the current unit's last softmax and epilogue.  Roles:
-//   warp 4        TMA producer: Q (two buffers), then K and V tiles (NST-stage ring)
+//   warp 4        TMA producer of Q (two buffers) and K (NST-stage ring)
+//   warp 7        TMA producer of V (NST-stage ring)
 //   warp 5        tcgen05 MMA issuer (one thread): S = Q K^T into TMEM
 //                 (double buffered), O += P V with P read from TMEM
 //   warp 6        waits on the MMAs' dependencies and gates warp 5
@@ -35,7 +36,7 @@ namespace bda {
 
 namespace {
 
-constexpr int kFwdThreads = 224;
+constexpr int kFwdThreads = 256;
 constexpr uint32_t kMmaGate = 1;  // named barrier between the MMA warp and its waiter
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // P0 at kColP, P1 at kColP + 64
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
@@ -157,54 +158,58 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     return n < it.r1_end ? n : it.r2_begin + (n - it.r1_end);
   };
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == 4 || warp == 7) {
+    // ----------------------------------------------------------- producers
+    // Warp 4 streams Q and K, warp 7 streams V.  With one producer, the load
+    // of K(g+1) queued behind the wait for V(g)'s buffer, and the gate of
+    // S(g+1) then waited on a late K.
+    const bool kprod = warp == 4;
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      int nq[2] = {0, 0}, nk[NST], nv[NST];  // copies issued per barrier (abort drain)
-      for (int s = 0; s < NST; ++s) nk[s] = nv[s] = 0;
+      if (kprod) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+      } else {
+        tma_prefetch_desc(&tm_v);
+      }
+      int nq[2] = {0, 0}, nx[NST];  // copies issued per barrier (abort drain)
+      for (int s = 0; s < NST; ++s) nx[s] = 0;
+      const int b_full = kprod ? L::B_KFULL : L::B_VFULL;
+      const int b_empty = kprod ? L::B_KEMPTY : L::B_VEMPTY;
+      const CUtensorMap* tm = kprod ? &tm_k : &tm_v;
+      const uint32_t ring = base + (kprod ? L::K : L::V);
       bool ok = true;
       int g = 0;  // key tiles streamed so far (all units)
       for (int k = 0, u; ok && (u = unit_of(k, n_units)) >= 0; ++k) {
         const Unit x = load_unit(u);
-        const int qb = k & 1;
-        if (k >= 2 && !mbar_wait(wc, bar(L::B_QEMPTY + qb), uint32_t((k >> 1) - 1) & 1u)) {
-          ok = false;
-          break;
+        if (kprod) {
+          const int qb = k & 1;
+          if (k >= 2 && !mbar_wait(wc, bar(L::B_QEMPTY + qb), uint32_t((k >> 1) - 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(L::B_QFULL + qb), L::TILE);
+          for (int c = 0; c < L::CH; ++c)
+            tma_load_3d(base + L::Q + qb * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + qb),
+                        c * 64, x.head0, x.it.q_row);
+          ++nq[qb];
         }
-        mbar_arrive_expect_tx(bar(L::B_QFULL + qb), L::TILE);
-        for (int c = 0; c < L::CH; ++c)
-          tma_load_3d(base + L::Q + qb * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + qb),
-                      c * 64, x.head0, x.it.q_row);
-        ++nq[qb];
         for (int n = 0; n < x.n_tiles; ++n, ++g) {
           const int s = g % NST;
           const uint32_t ph = uint32_t(g / NST) & 1u;
           const int krow = x.it.k_row + key_tile(x.it, n) * kTileN;
-          if (g >= NST && !mbar_wait(wc, bar(L::B_KEMPTY + s), ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(L::B_KFULL + s), L::TILE);
+          if (g >= NST && !mbar_wait(wc, bar(b_empty + s), ph ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(b_full + s), L::TILE);
           for (int c = 0; c < L::CH; ++c)
-            tma_load_3d(base + L::K + s * L::TILE + c * L::CHUNK, &tm_k, bar(L::B_KFULL + s),
-                        c * 64, x.kvh, krow);
-          ++nk[s];
-          if (g >= NST && !mbar_wait(wc, bar(L::B_VEMPTY + s), ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::TILE);
-          for (int c = 0; c < L::CH; ++c)
-            tma_load_3d(base + L::V + s * L::TILE + c * L::CHUNK, &tm_v, bar(L::B_VFULL + s),
-                        c * 64, x.kvh, krow);
-          ++nv[s];
+            tma_load_3d(ring + s * L::TILE + c * L::CHUNK, tm, bar(b_full + s), c * 64, x.kvh, krow);
+          ++nx[s];
         }
       }
       if (!ok || *abort_flag) {
         // Let every copy already issued land before the CTA can exit.
         for (int q = 0; q < 2; ++q)
           if (nq[q]) drain_wait(wc, bar(L::B_QFULL + q), uint32_t(nq[q] - 1) & 1u);
-        for (int s = 0; s < NST; ++s) {
-          if (nk[s]) drain_wait(wc, bar(L::B_KFULL + s), uint32_t(nk[s] - 1) & 1u);
-          if (nv[s]) drain_wait(wc, bar(L::B_VFULL + s), uint32_t(nv[s] - 1) & 1u);
-        }
+        for (int s = 0; s < NST; ++s)
+          if (nx[s]) drain_wait(wc, bar(b_full + s), uint32_t(nx[s] - 1) & 1u);
       }
     }
   } else if (warp == 5 || warp == 6) {
@@ -219,13 +224,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const bool issuer = warp == 5;
     auto gate = [&](bool wait_ok) -> bool { return named_bar_and(kMmaGate, 64, wait_ok); };
     auto wt = [&](int b, uint32_t parity) -> bool { return mbar_wait_warp(wc, bar(b), parity); };
+    auto wt2 = [&](int b1, uint32_t p1, int b2, uint32_t p2) -> bool {
+      return mbar_wait2_warp(wc, bar(b1), p1, bar(b2), p2);
+    };
     constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
     constexpr uint32_t idO = idesc_bf16(128, D, false, true);
     // S(g) waits for K(g) and for the softmax to have read S(g-2) out of its buffer.
     auto s_ready = [&](int g) -> bool {
       const int s = g % NST, b = g & 1;
-      return wt(L::B_KFULL + s, uint32_t(g / NST) & 1u) &&
-             (g < 2 || wt(L::B_SFREE + b, uint32_t((g >> 1) - 1) & 1u));
+      return g < 2 ? wt(L::B_KFULL + s, uint32_t(g / NST) & 1u)
+                   : wt2(L::B_SFREE + b, uint32_t((g >> 1) - 1) & 1u, L::B_KFULL + s,
+                         uint32_t(g / NST) & 1u);
     };
     auto issue_s = [&](int g, int qb, bool last_of_unit) {
       const int s = g % NST, b = g & 1;
@@ -262,8 +271,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // O += P V; the unit's first product overwrites O, so the previous
         // unit's epilogue must have read it out.
         const int s = g % NST;
-        if (!(go = gate(issuer || (wt(L::B_PFULL, uint32_t(g) & 1u) &&
-                                   wt(L::B_VFULL + s, uint32_t(g / NST) & 1u) &&
+        if (!(go = gate(issuer || (wt2(L::B_VFULL + s, uint32_t(g / NST) & 1u, L::B_PFULL,
+                                       uint32_t(g) & 1u) &&
                                    (n > 0 || k == 0 || wt(L::B_OFREE, uint32_t(k - 1) & 1u))))))
           break;
         if (issuer) {
@@ -304,7 +313,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float l = 0.f;            // running sum of P (relative to m_ref)
       for (int n = 0; n < x.n_tiles; ++n, ++g) {
         const int b = g & 1;
-        if (!mbar_wait_warp(wc, bar(L::B_SFULL + b), uint32_t(g >> 1) & 1u)) { ok = false; break; }
+        // S(g) and, for the P buffer b this tile writes, P V of tile g-2
+        // (read out of b); one paired wait.
+        const bool got = g < 2 ? mbar_wait_warp(wc, bar(L::B_SFULL + b), uint32_t(g >> 1) & 1u)
+                               : mbar_wait2_warp(wc, bar(L::B_ODONE + b), uint32_t((g - 2) >> 1) & 1u,
+                                                 bar(L::B_SFULL + b), uint32_t(g >> 1) & 1u);
+        if (!got) { ok = false; break; }
         tc_fence_after();
         // All of S at once: four loads in flight, one wait.
         float sv[kTileN];
@@ -364,14 +378,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
             tmem_st32(lane_addr + kColO + 32u * c, rr);
           }
-        }
-        // P buffer b was last read by P V of tile g-2.
-        if (g >= 2) {
-          if (!mbar_wait_warp(wc, bar(L::B_ODONE + b), uint32_t((g - 2) >> 1) & 1u)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
         }
         float rs[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in four chains
 #pragma unroll

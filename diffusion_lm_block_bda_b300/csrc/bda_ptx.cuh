@@ -89,9 +89,25 @@ __device__ __forceinline__ bool mbar_wait(WaitCtx w, uint32_t bar, uint32_t pari
   return mbar_wait_slow(w, bar, parity);
 }
 
+// Wait for two phases: both polls are issued before either result is read,
+// so their latencies overlap (a poll costs a few hundred cycles when the
+// shared-memory pipe is busy).  Put the barrier more likely complete first.
+__device__ __forceinline__ bool mbar_wait2(WaitCtx w, uint32_t b1, uint32_t p1, uint32_t b2,
+                                           uint32_t p2) {
+  const bool d1 = mbar_try_wait(b1, p1);
+  const bool d2 = mbar_try_wait(b2, p2);
+  if (d1 && d2) return true;
+  return (d1 || mbar_wait_slow(w, b1, p1)) && (d2 || mbar_wait_slow(w, b2, p2));
+}
+
 // Warp-collective variant: every lane waits, the outcome is warp-uniform.
 __device__ __forceinline__ bool mbar_wait_warp(WaitCtx w, uint32_t bar, uint32_t parity) {
   const bool ok = mbar_wait(w, bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool mbar_wait2_warp(WaitCtx w, uint32_t b1, uint32_t p1, uint32_t b2,
+                                                uint32_t p2) {
+  const bool ok = mbar_wait2(w, b1, p1, b2, p2);
   return __all_sync(0xffffffffu, ok);
 }
 
