@@ -153,10 +153,11 @@ bda_status bda_attn_fwd(const bda_problem* prob, const bda_mask_desc* mask, cons
   if (!q || !k || !v || !o || !lse) return BDA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return BDA_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_thd_map(&tq, q, s.d, s.hq, s.total_q, s.hg, s.tok) ||
       !make_thd_map(&tk, k, s.d, s.hkv, s.total_k, 1, kTileN) ||
-      !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN))
+      !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN) ||
+      !make_thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok))
     return tensor_map_error();
   FwdArgs a{};
   a.items = reinterpret_cast<const FwdItem*>(plan_ptr(ws) + kHeaderBytes);
@@ -172,7 +173,7 @@ bda_status bda_attn_fwd(const bda_problem* prob, const bda_mask_desc* mask, cons
   a.total_q = int(s.total_q);
   a.block = s.B;
   a.scale_log2 = s.scale * 1.4426950408889634f;
-  return cuda_status(launch_fwd(s.d, tq, tk, tv, a, s.n_fwd, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_fwd(s.d, tq, tk, tv, to, a, s.n_fwd, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 bda_status bda_attn_bwd_preprocess(const bda_problem* prob, const bda_mask_desc* mask,

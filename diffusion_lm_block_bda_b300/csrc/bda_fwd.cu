@@ -37,7 +37,8 @@ namespace bda {
 namespace {
 
 constexpr int kFwdThreads = 256;
-constexpr uint32_t kMmaGate = 1;  // named barrier between the MMA warp and its waiter
+constexpr uint32_t kMmaGate = 1;     // named barrier between the MMA warp and its waiter
+constexpr uint32_t kEpiBarrier = 2;  // named barrier of the softmax warps (epilogue)
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // P0 at kColP, P1 at kColP + 64
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
 
@@ -49,7 +50,8 @@ struct FwdLayout {
   static constexpr uint32_t Q = 0;               // two buffers
   static constexpr uint32_t K = Q + 2 * TILE;
   static constexpr uint32_t V = K + NST * TILE;
-  static constexpr uint32_t BAR = V + NST * TILE;
+  static constexpr uint32_t OSTG = V + NST * TILE;  // O staging for the TMA store
+  static constexpr uint32_t BAR = OSTG + TILE;
   // q_full[2], q_empty[2], k_full[NST], k_empty[NST], v_full[NST], v_empty[NST],
   // s_full[2], s_free[2], p_full, o_done[2] (per P buffer), o_free, drain
   static constexpr int B_QFULL = 0;
@@ -83,6 +85,15 @@ __device__ __forceinline__ bool drain_wait(WaitCtx w, uint32_t bar, uint32_t par
   return true;
 }
 
+// Bits of the columns [lo, hi) that fall in the 32-column word starting at w0.
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int w0) {
+  const int l = min(max(lo - w0, 0), 32), h = min(max(hi - w0, 0), 32);
+  if (h <= l) return 0u;
+  const uint32_t below_h = h == 32 ? 0xffffffffu : (1u << h) - 1u;
+  const uint32_t below_l = l == 32 ? 0xffffffffu : (1u << l) - 1u;
+  return below_h & ~below_l;
+}
+
 // The k-th unit (k = 0, 1, ...) of this CTA: units are dealt to the CTAs in
 // snake order over the longest-first list (forward in even rounds, backward
 // in odd ones), which evens out the CTAs' totals.  -1 past the end.
@@ -95,7 +106,8 @@ __device__ __forceinline__ int unit_of(int k, int n_units) {
 template <int D, int NST>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     bda_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const FwdArgs a) {
   using L = FwdLayout<D, NST>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -171,16 +183,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       } else {
         tma_prefetch_desc(&tm_v);
       }
-      int nq[2] = {0, 0}, nx[NST];  // copies issued per barrier (abort drain)
-      for (int s = 0; s < NST; ++s) nx[s] = 0;
+      int nq[2] = {0, 0}, ncopy[NST];  // copies issued per barrier (abort drain)
+      for (int s = 0; s < NST; ++s) ncopy[s] = 0;
       const int b_full = kprod ? L::B_KFULL : L::B_VFULL;
       const int b_empty = kprod ? L::B_KEMPTY : L::B_VEMPTY;
       const CUtensorMap* tm = kprod ? &tm_k : &tm_v;
       const uint32_t ring = base + (kprod ? L::K : L::V);
       bool ok = true;
       int g = 0;  // key tiles streamed so far (all units)
-      for (int k = 0, u; ok && (u = unit_of(k, n_units)) >= 0; ++k) {
-        const Unit x = load_unit(u);
+      Unit nx{};  // the next unit's descriptor, fetched one unit ahead
+      int u = unit_of(0, n_units);
+      if (u >= 0) nx = load_unit(u);
+      for (int k = 0; ok && u >= 0; ++k) {
+        const Unit x = nx;
+        u = unit_of(k + 1, n_units);
+        if (u >= 0) nx = load_unit(u);
         if (kprod) {
           const int qb = k & 1;
           if (k >= 2 && !mbar_wait(wc, bar(L::B_QEMPTY + qb), uint32_t((k >> 1) - 1) & 1u)) {
@@ -201,7 +218,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mbar_arrive_expect_tx(bar(b_full + s), L::TILE);
           for (int c = 0; c < L::CH; ++c)
             tma_load_3d(ring + s * L::TILE + c * L::CHUNK, tm, bar(b_full + s), c * 64, x.kvh, krow);
-          ++nx[s];
+          ++ncopy[s];
         }
       }
       if (!ok || *abort_flag) {
@@ -209,7 +226,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int q = 0; q < 2; ++q)
           if (nq[q]) drain_wait(wc, bar(L::B_QFULL + q), uint32_t(nq[q] - 1) & 1u);
         for (int s = 0; s < NST; ++s)
-          if (nx[s]) drain_wait(wc, bar(b_full + s), uint32_t(nx[s] - 1) & 1u);
+          if (ncopy[s]) drain_wait(wc, bar(b_full + s), uint32_t(ncopy[s] - 1) & 1u);
       }
     }
   } else if (warp == 5 || warp == 6) {
@@ -251,8 +268,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     };
     bool go = true;
     int g = 0;  // key tiles issued so far (all units)
-    for (int k = 0, u; go && (u = unit_of(k, n_units)) >= 0; ++k) {
-      const Unit x = load_unit(u);
+    Unit nx{};  // the next unit's descriptor, fetched one unit ahead
+    int u = unit_of(0, n_units);
+    if (u >= 0) nx = load_unit(u);
+    for (int k = 0; go && u >= 0; ++k) {
+      const Unit x = nx;
+      u = unit_of(k + 1, n_units);
+      if (u >= 0) nx = load_unit(u);
       const int qb = k & 1;
       if (!(go = gate(issuer || (wt(L::B_QFULL + qb, uint32_t(k >> 1) & 1u) && s_ready(g)))))
         break;
@@ -303,8 +325,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     int g = 0;  // key tiles consumed so far (all units)
-    for (int k = 0, u; ok && (u = unit_of(k, n_units)) >= 0; ++k) {
-      const Unit x = load_unit(u);
+    Unit nx{};  // the next unit's descriptor, fetched one unit ahead
+    int u = unit_of(0, n_units);
+    if (u >= 0) nx = load_unit(u);
+    for (int k = 0; ok && u >= 0; ++k) {
+      const Unit x = nx;
+      u = unit_of(k + 1, n_units);
+      if (u >= 0) nx = load_unit(u);
       const FwdItem& it = x.it;
       const bool row_valid = t_local < it.q_len;
       const int p = it.pos0 + (row_valid ? t_local : it.q_len - 1);
@@ -337,11 +364,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(L::B_SFREE + b));
         if (n >= it.n_full) {  // PARTIAL tile: mask from block indices
+          // Visible columns [0, ca) and [cb, ce) as four 32-bit masks, then
+          // one bit test per score (a three-way compare per score cost as
+          // much as the rest of the tile's softmax).
           const int k0 = key_tile(it, n) * kTileN;
           const int ca = rk.a - k0, cb = rk.b - k0, ce = rk.e - k0;
+          uint32_t keep[kTileN / 32];
+#pragma unroll
+          for (int w = 0; w < kTileN / 32; ++w)
+            keep[w] = range_bits(0, ca, 32 * w) | range_bits(cb, ce, 32 * w);
 #pragma unroll
           for (int j = 0; j < kTileN; ++j)
-            if (!(j < ca || (j >= cb && j < ce))) sv[j] = -INFINITY;
+            if (!(keep[j >> 5] & (1u << (j & 31)))) sv[j] = -INFINITY;
         }
         // Row max as eight independent chains (a single chain would be 127
         // dependent steps).
@@ -397,11 +431,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(L::B_PFULL));
       }
-      if (!ok) break;
       // Epilogue: O out of TMEM (then the next unit's first P V may
-      // overwrite it), O / l and LSE to global memory.
+      // overwrite it), O / l and LSE to global memory.  The four warps meet
+      // at a named barrier that also carries their verdicts, so a failed
+      // wait anywhere stops all of them here together.
       const int gl = g - 1;  // the unit's last key tile
-      if (!mbar_wait_warp(wc, bar(L::B_ODONE + (gl & 1)), uint32_t(gl >> 1) & 1u)) {
+      bool good = ok && mbar_wait_warp(wc, bar(L::B_ODONE + (gl & 1)), uint32_t(gl >> 1) & 1u);
+      good = named_bar_and(kEpiBarrier, 128, good);
+      if (!good) {
         ok = false;
         break;
       }
@@ -413,8 +450,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int c = 0; c < D / 32; ++c) tmem_ld_wait(ov[c]);
       tc_fence_before();
       mbar_arrive(bar(L::B_OFREE));
-      if (row_valid) {
-        const float inv_l = 1.f / l;
+      const float inv_l = 1.f / l;
+      if (it.q_len == (kTileM >> a.lg_hg)) {
+        // Whole tile: rows go to swizzled shared memory (conflict-free) and
+        // the TMA writes the tile (a store from each thread would hit 32
+        // rows per instruction).  The previous store must have read the
+        // staging buffer first.
+        if (r == 0) bulk_wait_read<0>();
+        named_bar_sync(kEpiBarrier, 128);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(__uint_as_float(ov[c][2 * j]) * inv_l,
+                                __uint_as_float(ov[c][2 * j + 1]) * inv_l);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(gbase + L::OSTG + (c >> 1) * L::CHUNK +
+                                      sw128_offset(r, 4 * (c & 1) + j)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(kEpiBarrier, 128);
+        if (r == 0) {
+          for (int c = 0; c < L::CH; ++c)
+            tma_store_3d(&tm_o, base + L::OSTG + c * L::CHUNK, 64 * c, x.head0, it.q_row);
+          bulk_commit();
+        }
+      } else if (row_valid) {
+        // The sequence's last, partial tile: the box would spill into the
+        // next sequence's rows, so each thread stores its own row.
         __nv_bfloat16* orow =
             a.o + (size_t(it.q_row + t_local) * a.hq + size_t(x.head0 + hh)) * size_t(D);
 #pragma unroll
@@ -429,11 +495,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int j = 0; j < 4; ++j)
             dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
+      }
+      if (row_valid) {
         const float lse2 = m_ref + log2f(l);
         a.lse[size_t(x.head0 + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
             lse2 * 0.69314718055994530942f;
       }
     }
+    if (r == 0) bulk_wait_all();  // the last O stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -457,7 +526,7 @@ int fwd_sm_count() {
 
 template <int D, int NST>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdArgs& a, int n_items, cudaStream_t stream) {
+                         const CUtensorMap& to, const FwdArgs& a, int n_items, cudaStream_t stream) {
   using L = FwdLayout<D, NST>;
   static_assert(L::ALLOC <= 232448, "forward shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(bda_fwd_kernel<D, NST>,
@@ -466,17 +535,18 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   FwdArgs args = a;
   args.n_units = n_items * a.n_groups;
   const int grid = args.n_units < fwd_sm_count() ? args.n_units : fwd_sm_count();
-  bda_fwd_kernel<D, NST><<<unsigned(grid), kFwdThreads, L::ALLOC, stream>>>(tq, tk, tv, args);
+  bda_fwd_kernel<D, NST><<<unsigned(grid), kFwdThreads, L::ALLOC, stream>>>(tq, tk, tv, to, args);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const FwdArgs& a, int n_items, cudaStream_t stream) {
+                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, int n_items,
+                       cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
-  if (head_dim == 128) return launch_fwd_t<128, 2>(tq, tk, tv, a, n_items, stream);
-  return launch_fwd_t<64, 2>(tq, tk, tv, a, n_items, stream);
+  if (head_dim == 128) return launch_fwd_t<128, 2>(tq, tk, tv, to, a, n_items, stream);
+  return launch_fwd_t<64, 2>(tq, tk, tv, to, a, n_items, stream);
 }
 
 }  // namespace bda

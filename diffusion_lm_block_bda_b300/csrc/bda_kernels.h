@@ -42,8 +42,11 @@ struct BwdArgs {
   float scale_log2;  // softmax_scale * log2(e)
 };
 
+// to: map over O laid out like Q (box 64 x hg x tok, 128-byte swizzle); whole
+// query tiles are written through it.
 cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const FwdArgs& a, int n_items, cudaStream_t stream);
+                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, int n_items,
+                       cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(int head_dim, const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                   float* D, float* dq_acc, int64_t total_q, int hq,

@@ -114,10 +114,11 @@ bda_status bda_attn_fwd_noalloc(const bda_problem* prob, const bda_mask_desc* ma
   if (!q || !k || !v || !o || !lse) return BDA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return BDA_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!thd_map(&tq, q, s.d, s.hq, s.total_q, s.hg, s.tok) ||
       !thd_map(&tk, k, s.d, s.hkv, s.total_k, 1, kTileN) ||
-      !thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN)) {
+      !thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN) ||
+      !thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok)) {
     note_cuda_error("cuTensorMapEncodeTiled failed");
     return BDA_ERR_CUDA;
   }
@@ -144,7 +145,7 @@ bda_status bda_attn_fwd_noalloc(const bda_problem* prob, const bda_mask_desc* ma
   a.total_q = int(s.total_q);
   a.block = s.B;
   a.scale_log2 = s.scale * 1.4426950408889634f;
-  e = launch_fwd(s.d, tq, tk, tv, a, s.n_fwd, cs);
+  e = launch_fwd(s.d, tq, tk, tv, to, a, s.n_fwd, cs);
   if (e != cudaSuccess) return fail_cuda(e);
   return BDA_OK;
 }

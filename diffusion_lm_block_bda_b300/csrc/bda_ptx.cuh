@@ -126,6 +126,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Store a shared-memory tile to global memory through a tensor map
+// (completion tracked by the issuing thread's bulk async-groups).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 // Element-wise add of a shared-memory tile into global memory through a
 // tensor map (the reduction is performed by the TMA unit, atomically per
 // element); completion is tracked by the issuing thread's bulk async-groups.
