@@ -45,40 +45,47 @@ __global__ void __launch_bounds__(256) bda_bwd_preprocess_kernel(const __nv_bflo
                                                                  float* __restrict__ Dv,
                                                                  float* __restrict__ dq_acc,
                                                                  int64_t total_q, int hq) {
-  constexpr int PER = D / 32;  // elements per lane
+  // A row is D/8 lanes x 16 bytes; each warp loads NR rows of O and dO
+  // before reducing any (one row at a time leaves the loads latency-bound).
+  constexpr int LPR = D / 8, RPI = 32 / LPR, NR = 8, NI = NR / RPI;
   const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, col = (lane % LPR) * 8;
   const int64_t rows = total_q * hq;
   const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t row = warp0; row < rows; row += nwarps) {
-    const __nv_bfloat16* po = o + row * D + lane * PER;
-    const __nv_bfloat16* pd = dout + row * D + lane * PER;
-    float acc = 0.f;
-    if constexpr (PER == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(po);
-      const uint2 b = *reinterpret_cast<const uint2*>(pd);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  for (int64_t r0 = warp0 * NR; r0 < rows; r0 += nwarps * NR) {
+    uint4 xo[NI], xd[NI];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float2 x = __bfloat1622float2(a2[j]), y = __bfloat1622float2(b2[j]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
+    for (int i = 0; i < NI; ++i) {
+      const int64_t row = r0 + i * RPI + sub;
+      if (row < rows) {
+        xo[i] = *reinterpret_cast<const uint4*>(o + row * D + col);
+        xd[i] = *reinterpret_cast<const uint4*>(dout + row * D + col);
       }
-      *reinterpret_cast<float4*>(dq_acc + row * D + lane * PER) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(po);
-      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(pd);
-      const float2 x = __bfloat1622float2(a), y = __bfloat1622float2(b);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
-      *reinterpret_cast<float2*>(dq_acc + row * D + lane * PER) = make_float2(0.f, 0.f);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-      const int64_t t = row / hq, h = row - t * hq;
-      Dv[h * total_q + t] = acc;
+    for (int i = 0; i < NI; ++i) {
+      const int64_t row = r0 + i * RPI + sub;
+      float acc = 0.f;
+      if (row < rows) {
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&xo[i]);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&xd[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 x = __bfloat1622float2(a2[j]), y = __bfloat1622float2(b2[j]);
+          acc = fmaf(x.x, y.x, acc);
+          acc = fmaf(x.y, y.y, acc);
+        }
+        float4* z = reinterpret_cast<float4*>(dq_acc + row * D + col);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (row < rows && lane % LPR == 0) {
+        const int64_t t = row / hq, h = row - t * hq;
+        Dv[h * total_q + t] = acc;
+      }
     }
   }
 }
@@ -655,8 +662,8 @@ cudaError_t launch_bwd_preprocess(int head_dim, const __nv_bfloat16* o, const __
                                   cudaStream_t stream) {
   const int64_t rows = total_q * hq;
   if (rows == 0) return cudaSuccess;
-  int64_t blocks = (rows + 7) / 8;  // 8 warps per block, one row per warp per pass
-  const int64_t cap = int64_t(sm_count()) * 16;
+  int64_t blocks = (rows + 63) / 64;  // 8 warps per block, 8 rows per warp per pass
+  const int64_t cap = int64_t(sm_count()) * 8;  // 64 warps per SM
   if (blocks > cap) blocks = cap;
   if (head_dim == 128)
     bda_bwd_preprocess_kernel<128><<<unsigned(blocks), 256, 0, stream>>>(o, dout, D, dq_acc, total_q, hq);

@@ -66,6 +66,75 @@ def test_edge_cases_full_oracle(case):
     compare_full(w, inp, got)
 
 
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+def _poison_dq_accumulator(ws, w, total_q):
+    """Fill the workspace's fp32 dQ accumulator with NaN, so any row left
+    unzeroed before a backward shows up.  A backward-sized workspace ends
+    with the accumulator [total_q][hq][d]."""
+    ws[ws.numel() - _align256(4 * total_q * w.hq * w.head_dim):].fill_(0xFF)
+
+
+@pytest.mark.parametrize("case", [(BC, 16, 8, 2, 128, [1, 7, 130, 257, 33], None),
+                                  (SC, 16, 8, 2, 64, [160, 96], [32, 0])],
+                         ids=["bc_d128", "sc_d64"])
+def test_dq_accumulator_reuse(case):
+    """Each backward clears the workspace's dQ accumulator itself: garbage left
+    there (NaN poison, or the sums of an earlier backward) never reaches dQ,
+    whether or not a forward ran on the workspace first."""
+    from diffusion_lm_block_bda_b300 import Attention, Problem
+    kind, B, hq, hkv, d, lq, prefix = case
+    w = W.custom(kind, B, hq, hkv, d, lq, None, prefix, name=f"dqacc_{kind}_{d}")
+    inp = W.make_inputs(w, seed=5)
+    pb = Problem.from_workload(w)
+    q, k, v, dout = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
+    att = Attention(pb, device="cuda", with_bwd=True)
+    _poison_dq_accumulator(att.ws, w, pb.total_q)
+    o, lse = att.forward(q, k, v)
+    runs = [att.backward(q, k, v, o, lse, dout)]
+    runs.append(att.backward(q, k, v, o, lse, dout))  # no forward between
+    fresh = Attention(pb, device="cuda", with_bwd=True)
+    _poison_dq_accumulator(fresh.ws, w, pb.total_q)
+    runs.append(fresh.backward(q, k, v, o, lse, dout))  # backward only
+    torch.cuda.synchronize()
+    att.check()
+    fresh.check()
+    for dq, dk, dv in runs:
+        got = dict(o=o.float().cpu(), lse=lse.float().cpu(), dq=dq.float().cpu(),
+                   dk=dk.float().cpu(), dv=dv.float().cpu())
+        compare_full(w, inp, got)
+
+
+def test_workspace_reused_across_problems():
+    """One workspace, two packed batches of different lengths back to back
+    (plan, forward, backward each): the second backward relies on the first
+    leaving the dQ accumulator clear, as it does for every backward."""
+    import diffusion_lm_block_bda_b300 as bda
+    from diffusion_lm_block_bda_b300 import Problem
+    ws_list = [W.custom(BC, 32, 8, 2, 128, [300, 64, 450], name="reuse_a"),
+               W.custom(BC, 32, 8, 2, 128, [128, 513, 97], name="reuse_b"),
+               W.custom(SC, 32, 8, 2, 128, [416, 160], prefix=[96, 64], name="reuse_c")]
+    pbs = [Problem.from_workload(w) for w in ws_list]
+    size = max(bda.bda_attn_workspace_size(pb, True) for pb in pbs)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    for w, pb in zip(ws_list * 2, pbs * 2):
+        inp = W.make_inputs(w, seed=7)
+        host = torch.empty(bda.bda_attn_plan_size(pb), dtype=torch.uint8).pin_memory()
+        bda.bda_attn_plan(pb, host, ws)
+        q, k, v, dout = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((w.hq, pb.total_q), float("nan"), device="cuda")
+        dq, dk, dv = (torch.full_like(x, float("nan")) for x in (q, k, v))
+        bda.bda_attn_fwd(pb, q, k, v, o, lse, ws)
+        bda.bda_attn_bwd(pb, q, k, v, o, lse, dout, dq, dk, dv, ws)
+        torch.cuda.synchronize()
+        assert bda.bda_attn_check_status(ws) == bda.BDA_OK
+        got = {n: t.float().cpu() for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
+        compare_full(w, inp, got)
+
+
 def test_staircase_replay_c4():
     w = W.named("c4")
     inp = W.make_inputs(w, seed=0)
