@@ -11,7 +11,9 @@ stages, on inputs already resident in HBM.  `value` counts useful FLOPs only
 (4 d Hq pairs forward + 10 d Hq pairs backward, pairs = allowed (query, key)
 pairs).  `e2e` repeats the step through the same public API with the inputs
 copied from pinned host memory and every output (O, LSE, dQ, dK, dV) copied
-back inside the timed region.  With N > 1 (torchrun, one rank per GPU) the
+back inside the timed region; as in a training loop that prefetches its next
+batch, the copies run on two copy streams and overlap the neighbouring steps'
+compute (two device buffer sets).  With N > 1 (torchrun, one rank per GPU) the
 global batch holds 16 N sequences, sharded whole by longest-first load
 balancing with no collective on the data path (weak scaling); the timing is
 the max over ranks.
@@ -303,22 +305,25 @@ def main():
         ring_ev[b] = ev
         step_no[0] += 1
 
-    def step(evs=None):
+    def step(evs=None, io=None):
+        i_, o_ = io if io is not None else (dict(q=q, k=k, v=v, dout=dout),
+                                            dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv))
         if evs:
             evs[0].record(stream)
         plan()
         if evs:
             evs[1].record(stream)
-        bda.bda_attn_fwd(pb, q, k, v, o, lse, ws, stream)
+        bda.bda_attn_fwd(pb, i_["q"], i_["k"], i_["v"], o_["o"], o_["lse"], ws, stream)
         if evs:
             evs[2].record(stream)
-        bda.bda_attn_bwd_preprocess(pb, o, dout, ws, stream)
+        bda.bda_attn_bwd_preprocess(pb, o_["o"], i_["dout"], ws, stream)
         if evs:
             evs[3].record(stream)
-        bda.bda_attn_bwd_dkdv(pb, q, k, v, lse, dout, dk, dv, ws, stream)
+        bda.bda_attn_bwd_dkdv(pb, i_["q"], i_["k"], i_["v"], o_["lse"], i_["dout"], o_["dk"],
+                              o_["dv"], ws, stream)
         if evs:
             evs[4].record(stream)
-        bda.bda_attn_bwd_dq_convert(pb, dq, ws, stream)
+        bda.bda_attn_bwd_dq_convert(pb, o_["dq"], ws, stream)
         if evs:
             evs[5].record(stream)
 
@@ -348,44 +353,70 @@ def main():
     stage_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j in range(5)]
     gpu_launches = 4 * K
 
-    # ---- end-to-end through the public API with host buffers
+    # ---- end-to-end through the public API with host buffers.  Every step
+    # uploads its inputs from pinned host memory and downloads all of its
+    # outputs; as a training loop would, the upload of step j+1 and the
+    # download of step j-1 run on their own streams while step j computes
+    # (two device buffer sets, ordered by events).
     e2e = None
     if not args.no_e2e:
         host_in = {n: inp[n].pin_memory() for n in ("q", "k", "v", "dout")}
-        host_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
-                    "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
-                    "dq": torch.empty(dq.shape, dtype=dq.dtype).pin_memory(),
-                    "dk": torch.empty(dk.shape, dtype=dk.dtype).pin_memory(),
-                    "dv": torch.empty(dv.shape, dtype=dv.dtype).pin_memory()}
-        dev_in = {"q": q, "k": k, "v": v, "dout": dout}
-        dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        out_like = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        host_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in out_like.items()}
+        sets = [({"q": q, "k": k, "v": v, "dout": dout}, out_like)]
+        sets.append(({n: torch.empty_like(t) for n, t in sets[0][0].items()},
+                     {n: torch.empty_like(t) for n, t in out_like.items()}))
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        in_ready = [torch.cuda.Event() for _ in sets]
+        in_free = [torch.cuda.Event() for _ in sets]
+        out_free = [torch.cuda.Event() for _ in sets]
+        computed = [torch.cuda.Event() for _ in sets]
+        for e in in_free + out_free:
+            e.record(stream)
 
-        def e2e_step():
-            for n, t in host_in.items():
-                dev_in[n].copy_(t, non_blocking=True)
-            step()
-            for n, t in host_out.items():
-                t.copy_(dev_out[n], non_blocking=True)
+        def e2e_step(j):
+            b = j % 2
+            di, do = sets[b]
+            with torch.cuda.stream(s_h2d):
+                s_h2d.wait_event(in_free[b])
+                for n, t in host_in.items():
+                    di[n].copy_(t, non_blocking=True)
+                in_ready[b].record(s_h2d)
+            stream.wait_event(in_ready[b])
+            stream.wait_event(out_free[b])
+            step(io=(di, do))
+            computed[b].record(stream)
+            in_free[b].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(computed[b])
+                for n, t in host_out.items():
+                    t.copy_(do[n], non_blocking=True)
+                out_free[b].record(s_d2h)
 
-        for _ in range(2):
-            e2e_step()
+        for j in range(2):
+            e2e_step(j)
         torch.cuda.synchronize()
         K2 = max(3, min(K, 20))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
         e0.record(stream)
-        for _ in range(K2):
-            e2e_step()
+        s_h2d.wait_event(e0)
+        s_d2h.wait_event(e0)
+        for j in range(K2):
+            e2e_step(j)
+        for e in out_free:
+            stream.wait_event(e)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K2, world)
         e2e_flops = sum_over_ranks(step_flops, world)
         e2e = {"value": e2e_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K2,
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms,
+               "overlap": "step j+1 upload and step j-1 download overlap step j (3 streams)"}
     clocks = clk.stop()
     status = bda.bda_attn_check_status(ws, stream)
     if status != bda.BDA_OK:
