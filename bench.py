@@ -13,7 +13,9 @@ pairs).  `e2e` repeats the step through the same public API with the inputs
 copied from pinned host memory and every output (O, LSE, dQ, dK, dV) copied
 back inside the timed region; as in a training loop that prefetches its next
 batch, the copies run on two copy streams and overlap the neighbouring steps'
-compute (two device buffer sets).  With N > 1 (torchrun, one rank per GPU) the
+compute (two device buffer sets).  `decode` times the HBM-bound decode step
+(32 queries over 2,080 keys, forward only) against the measured copy
+bandwidth, and its replay from a captured CUDA graph.  With N > 1 (torchrun, one rank per GPU) the
 global batch holds 16 N sequences, sharded whole by longest-first load
 balancing with no collective on the data path (weak scaling); the timing is
 the max over ranks.
@@ -53,6 +55,7 @@ def parse():
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-decode", action="store_true")
     return p.parse_args()
 
 
@@ -260,6 +263,68 @@ def cpu_baseline(w, inp):
                       f"{t:.1f} s"}
 
 
+# ------------------------------------------------------------------ decode
+def decode_measurement(bda, dev, stream, hbm_gbs, reps=50):
+    """The decode step (32 new queries over a 2,080-key context: 2,048
+    committed tokens + the active block; Hq=32, Hkv=8, d=128; forward only)
+    is bound by HBM bandwidth and latency, not by the tensor cores.  One
+    forward launch is timed with CUDA events after a write of 256 MB (twice
+    L2) so its K/V come from HBM; `achieved` divides the minimum bytes (Q, K,
+    V read once, O and LSE written) by the median launch time.  The same
+    forward is then captured once in a CUDA graph and replayed: `graph_us` is
+    the per-round latency of a captured denoising loop (L2 warm, as when the
+    rounds revisit one KV cache)."""
+    from diffusion_lm_block_bda_b300 import Problem
+    w = W.named("c2")
+    inp = W.make_inputs(w, seed=0, with_dout=False)
+    pb = Problem.from_workload(w)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.hq, pb.total_q), dtype=torch.float32, device=dev)
+    ws = torch.zeros(bda.bda_attn_workspace_size(pb, False), dtype=torch.uint8, device=dev)
+    host = torch.empty(bda.bda_attn_plan_size(pb), dtype=torch.uint8).pin_memory()
+    bda.bda_attn_plan(pb, host, ws, stream)
+    nbytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, lse))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(5):
+        bda.bda_attn_fwd(pb, q, k, v, o, lse, ws, stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record(stream)
+        bda.bda_attn_fwd(pb, q, k, v, o, lse, ws, stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    cold_ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    # CUDA graph: the plan is in the workspace already; capture the launch.
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        bda.bda_attn_fwd(pb, q, k, v, o, lse, ws, cap)
+    rounds = 200
+    for _ in range(10):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(cap)
+    for _ in range(rounds):
+        graph.replay()
+    g1.record(cap)
+    torch.cuda.synchronize()
+    st = bda.bda_attn_check_status(ws, stream)
+    if st != bda.BDA_OK:
+        raise SystemExit(f"device status {st} after the decode measurement")
+    achieved = nbytes / (cold_ms * 1e-3) / 1e9
+    return {"workload": "decode step: 32 queries over 2,080 keys (2,048 + one block of 32), "
+                        "Hq=32, Hkv=8, d=128, forward only",
+            "bound": "hbm", "bytes": nbytes, "us": cold_ms * 1e3, "achieved": achieved,
+            "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+            "l2": "256 MB written before each timed launch",
+            "graph_us": g0.elapsed_time(g1) * 1e3 / rounds, "graph_rounds": rounds}
+
+
 # ------------------------------------------------------------------ native
 def main():
     args = parse()
@@ -458,6 +523,8 @@ def main():
     out["bwd_tflops"] = bwd_flops / (sum(stage_ms[2:]) * 1e-3) / 1e12
     if e2e is not None:
         out["e2e"] = e2e
+    if not args.no_decode:
+        out["decode"] = decode_measurement(bda, dev, stream, hbm)
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, inp)
     print(json.dumps(out), flush=True)

@@ -135,6 +135,56 @@ def test_workspace_reused_across_problems():
         compare_full(w, inp, got)
 
 
+def test_forward_and_backward_replay_from_cuda_graph():
+    """After bda_attn_plan, forward and backward are capturable: replaying the
+    captured launches reproduces the eager results bit for bit (no kernel
+    uses atomics whose order varies, except the dQ accumulation, compared
+    within the parity tolerance)."""
+    import diffusion_lm_block_bda_b300 as bda
+    from diffusion_lm_block_bda_b300 import Problem
+    for w, bwd in ((W.named("c2"), False),
+                   (W.custom(SC, 32, 8, 2, 128, [416, 160], prefix=[96, 64], name="graph_sc"), True)):
+        inp = W.make_inputs(w, seed=11)
+        pb = Problem.from_workload(w)
+        q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+        ws = torch.zeros(bda.bda_attn_workspace_size(pb, bwd), dtype=torch.uint8, device="cuda")
+        host = torch.empty(bda.bda_attn_plan_size(pb), dtype=torch.uint8).pin_memory()
+        bda.bda_attn_plan(pb, host, ws)
+        outs = []
+        for captured in (False, True):
+            o = torch.full_like(q, float("nan"))
+            lse = torch.full((w.hq, pb.total_q), float("nan"), device="cuda")
+            grads = [torch.full_like(x, float("nan")) for x in (q, k, v)] if bwd else []
+            dout = inp["dout"].cuda() if bwd else None
+
+            def run(stream=None):
+                bda.bda_attn_fwd(pb, q, k, v, o, lse, ws, stream)
+                if bwd:
+                    bda.bda_attn_bwd(pb, q, k, v, o, lse, dout, *grads, ws, stream)
+
+            if captured:
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    run(s)
+                g.replay()
+                g.replay()
+            else:
+                run()
+            torch.cuda.synchronize()
+            assert bda.bda_attn_check_status(ws) == bda.BDA_OK
+            outs.append([t.float().cpu() for t in [o, lse] + grads])
+        eager, graphed = outs
+        assert torch.equal(eager[0], graphed[0]) and torch.equal(eager[1], graphed[1])
+        if bwd:
+            assert torch.equal(eager[3], graphed[3]) and torch.equal(eager[4], graphed[4])
+            got = dict(o=graphed[0], lse=graphed[1], dq=graphed[2], dk=graphed[3], dv=graphed[4])
+            compare_full(w, inp, got)
+        else:
+            compare_full(w, inp, dict(o=graphed[0], lse=graphed[1]), with_bwd=False)
+
+
 def test_staircase_replay_c4():
     w = W.named("c4")
     inp = W.make_inputs(w, seed=0)
