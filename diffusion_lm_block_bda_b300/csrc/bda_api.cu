@@ -173,14 +173,7 @@ bda_status bda_attn_fwd(const bda_problem* prob, const bda_mask_desc* mask, cons
   a.total_q = int(s.total_q);
   a.block = s.B;
   a.scale_log2 = s.scale * 1.4426950408889634f;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  a.part_o = reinterpret_cast<float*>(w + ws_offset_parts(s));
-  a.part_lse = a.part_o + size_t(s.n_parts) * size_t(s.hq / s.hg) * size_t(kTileM) * size_t(s.d);
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  bda_status r = cuda_status(launch_fwd(s.d, tq, tk, tv, to, a, s.n_fwd, cs));
-  if (r != BDA_OK || s.n_comb == 0) return r;
-  return cuda_status(launch_fwd_combine(
-      s.d, reinterpret_cast<const CombItem*>(plan_ptr(ws) + plan_offset_comb(s)), s.n_comb, a, cs));
+  return cuda_status(launch_fwd(s.d, tq, tk, tv, to, a, s.n_fwd, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 bda_status bda_attn_bwd_preprocess(const bda_problem* prob, const bda_mask_desc* mask,

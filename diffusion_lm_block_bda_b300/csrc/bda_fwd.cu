@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     return x;
   };
   auto key_tile = [](const FwdItem& it, int n) -> int {
-    return n < it.r1_end ? it.kt_off + n : it.r2_begin + (n - it.r1_end);
+    return n < it.r1_end ? n : it.r2_begin + (n - it.r1_end);
   };
 
   if (warp == 4 || warp == 7) {
@@ -451,21 +451,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(L::B_OFREE));
       const float inv_l = 1.f / l;
-      if (it.part >= 0) {
-        // One split of the tile's key tiles: its normalised O and LSE (log2
-        // units) go to the workspace, row-fastest so the stores of a warp
-        // and the combine kernel's loads are contiguous.
-        if (row_valid) {
-          const size_t slot = size_t(it.part) * size_t(a.n_groups) + size_t(x.head0 >> a.lg_hg);
-          float* po = a.part_o + slot * size_t(D) * kTileM + r;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              po[size_t(32 * c + j) * kTileM] = __uint_as_float(ov[c][j]) * inv_l;
-          a.part_lse[slot * kTileM + r] = m_ref + log2f(l);
-        }
-      } else if (it.q_len == (kTileM >> a.lg_hg)) {
+      if (it.q_len == (kTileM >> a.lg_hg)) {
         // Whole tile: rows go to swizzled shared memory (conflict-free) and
         // the TMA writes the tile (a store from each thread would hit 32
         // rows per instruction).  The previous store must have read the
@@ -510,7 +496,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
-      if (row_valid && it.part < 0) {
+      if (row_valid) {
         const float lse2 = m_ref + log2f(l);
         a.lse[size_t(x.head0 + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
             lse2 * 0.69314718055994530942f;
@@ -525,47 +511,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
-}
-
-// Merges the splits of a query tile: with LSE_s in log2 units,
-//   M = max_s LSE_s,  w_s = 2^(LSE_s - M),  O = sum_s w_s O_s / sum_s w_s,
-//   LSE = (M + log2 sum_s w_s) ln 2.
-// One block per (split query tile, head group), thread r = tile row r.
-template <int D>
-__global__ void __launch_bounds__(kTileM) bda_fwd_combine_kernel(const CombItem* __restrict__ items,
-                                                                 const float* __restrict__ part_o,
-                                                                 const float* __restrict__ part_lse,
-                                                                 __nv_bfloat16* __restrict__ o,
-                                                                 float* __restrict__ lse, int n_groups,
-                                                                 int hg, int lg_hg, int hq, int total_q) {
-  const int ci = blockIdx.x / n_groups, grp = blockIdx.x - ci * n_groups;
-  const CombItem c = items[ci];
-  const int r = threadIdx.x, t = r >> lg_hg, hh = r & (hg - 1);
-  if (t >= c.q_len) return;
-  auto slot = [&](int s) -> size_t { return size_t(c.part0 + s) * size_t(n_groups) + size_t(grp); };
-  float M = -INFINITY;
-  for (int s = 0; s < c.n_part; ++s) M = fmaxf(M, part_lse[slot(s) * kTileM + r]);
-  float L = 0.f;
-  for (int s = 0; s < c.n_part; ++s) L += exp2f(part_lse[slot(s) * kTileM + r] - M);
-  const float inv_L = 1.f / L;
-  __nv_bfloat16* orow = o + (size_t(c.q_row + t) * size_t(hq) + size_t(grp * hg + hh)) * size_t(D);
-  for (int c0 = 0; c0 < D; c0 += 8) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < c.n_part; ++s) {
-      const float w = exp2f(part_lse[slot(s) * kTileM + r] - M);
-      const float* ps = part_o + (slot(s) * size_t(D) + size_t(c0)) * kTileM + r;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, ps[size_t(j) * kTileM], acc[j]);
-    }
-    uint4 v;
-    v.x = pack_bf16x2(acc[0] * inv_L, acc[1] * inv_L);
-    v.y = pack_bf16x2(acc[2] * inv_L, acc[3] * inv_L);
-    v.z = pack_bf16x2(acc[4] * inv_L, acc[5] * inv_L);
-    v.w = pack_bf16x2(acc[6] * inv_L, acc[7] * inv_L);
-    *reinterpret_cast<uint4*>(orow + c0) = v;
-  }
-  lse[size_t(grp * hg + hh) * size_t(total_q) + size_t(c.q_row + t)] =
-      (M + log2f(L)) * 0.69314718055994530942f;
 }
 
 int fwd_sm_count() {
@@ -602,21 +547,6 @@ cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& t
   if (n_items == 0) return cudaSuccess;
   if (head_dim == 128) return launch_fwd_t<128, 2>(tq, tk, tv, to, a, n_items, stream);
   return launch_fwd_t<64, 2>(tq, tk, tv, to, a, n_items, stream);
-}
-
-cudaError_t launch_fwd_combine(int head_dim, const CombItem* items, int n_comb, const FwdArgs& a,
-                               cudaStream_t stream) {
-  if (n_comb == 0) return cudaSuccess;
-  const unsigned grid = unsigned(n_comb) * unsigned(a.n_groups);
-  if (head_dim == 128)
-    bda_fwd_combine_kernel<128><<<grid, kTileM, 0, stream>>>(items, a.part_o, a.part_lse, a.o, a.lse,
-                                                             a.n_groups, a.hg, a.lg_hg, a.hq,
-                                                             a.total_q);
-  else
-    bda_fwd_combine_kernel<64><<<grid, kTileM, 0, stream>>>(items, a.part_o, a.part_lse, a.o, a.lse,
-                                                            a.n_groups, a.hg, a.lg_hg, a.hq,
-                                                            a.total_q);
-  return cudaGetLastError();
 }
 
 }  // namespace bda

@@ -17,25 +17,17 @@ struct Shape {
   int kind = 0, B = 1;
   float scale = 0.f;
   int64_t total_q = 0, total_k = 0;
-  int n_fwd = 0;    // forward work items (query tiles, or splits of them)
+  int n_fwd = 0;    // forward work items (query tiles)
   int n_bwd = 0;    // backward work items (key tiles)
-  int split = 0;    // splits wanted per query tile (0: none)
-  int n_comb = 0;   // query tiles split into partial items
-  int n_parts = 0;  // partial-output slots (items that are splits)
 };
 
 // Validates the problem and mask; fills `s`.  Host-only, launches nothing.
-// allow_split = false keeps one forward item per query tile (no partial
-// outputs, for callers without a workspace to hold them).
-bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s,
-                    bool allow_split = true);
+bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s);
 
 size_t plan_bytes(const Shape& s);
 size_t workspace_bytes(const Shape& s, bool with_bwd);
-size_t ws_offset_parts(const Shape& s);  // fp32 split outputs: O [part][group][d][128], LSE
 size_t ws_offset_D(const Shape& s);      // fp32 [hq][total_q]
 size_t ws_offset_dqacc(const Shape& s);  // fp32 [total_q][hq][d]
-size_t plan_offset_comb(const Shape& s);  // CombItem[n_comb] inside the plan
 
 // Writes the header and the LPT-ordered work items into `out` (plan_bytes).
 void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, uint8_t* out);

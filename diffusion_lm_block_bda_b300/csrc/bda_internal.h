@@ -28,10 +28,8 @@ constexpr uint32_t kPlanMagic = 0x42444131u;  // "BDA1"
 constexpr int kHeaderBytes = 256;
 
 // One forward work unit: a query tile (tok tokens of one sequence x hg query
-// heads) and the key tiles it visits: kt_off + [0, r1_end), then
-// [r2_begin, r2_end); the first n_full of them need no mask.  An item with
-// part >= 0 is one split of its query tile's key tiles: it writes a partial
-// O and LSE to the workspace for the combine kernel instead of O and LSE.
+// heads); its key tiles are [0, r1_end) then [r2_begin, r2_end); tiles below
+// n_full need no mask.
 struct FwdItem {
   int32_t q_row;     // global row of the tile's first query token
   int32_t q_len;     // valid query tokens in the tile (1..tok)
@@ -39,32 +37,15 @@ struct FwdItem {
   int32_t k_row;     // global row of the sequence's first key
   int32_t lk;        // keys in the sequence
   int32_t prefix;    // staircase prefix length; lk for block-causal
-  int32_t n_full;    // visited tiles [0, n_full) are FULL
-  int32_t r1_end;    // visited tiles [n_full, r1_end) are PARTIAL
+  int32_t n_full;    // key tiles [0, n_full) are FULL
+  int32_t r1_end;    // key tiles [n_full, r1_end) are PARTIAL
   int32_t r2_begin;  // key tiles [r2_begin, r2_end) are PARTIAL
   int32_t r2_end;
   int32_t work;      // number of key tiles
   int32_t seq;
-  int32_t kt_off;    // key tile of visited tile 0 (0 unless a later split)
-  int32_t part;      // partial-output slot of a split, -1 otherwise
-  int32_t pad[2];
+  int32_t pad[4];
 };
 static_assert(sizeof(FwdItem) == 64, "FwdItem layout");
-
-// A query tile whose key tiles were split: its partial slots are
-// [part0, part0 + n_part); the combine kernel merges them into O and LSE.
-struct CombItem {
-  int32_t q_row;
-  int32_t q_len;
-  int32_t part0;
-  int32_t n_part;
-};
-static_assert(sizeof(CombItem) == 16, "CombItem layout");
-// Splitting applies when a problem has fewer than half as many forward units
-// (query tiles x head groups) as this many SMs (B300: 148); splits per tile
-// are capped so the combine kernel's loop stays short.
-constexpr int kSplitTargetUnits = 148;
-constexpr int kMaxSplits = 32;
 
 // One backward work unit: a 128-key tile of one sequence (all KV heads run it
 // in parallel); query tokens [q_begin, q_end) are the ones that see it.
@@ -93,8 +74,6 @@ struct PlanHeader {
   int32_t tok;
   int32_t total_q;
   int32_t total_k;
-  int32_t n_comb;    // query tiles split into partial items
-  int32_t n_parts;   // partial-output slots
 };
 
 // Keys visible to the query at position p: [0, a) U [b, e).

@@ -24,8 +24,6 @@ struct FwdArgs {
   int total_q;
   int block;
   float scale_log2;  // softmax_scale * log2(e)
-  float* part_o;     // split outputs: O fp32 [part][group][d][128 rows]
-  float* part_lse;   // split outputs: LSE (log2 units) fp32 [part][group][128 rows]
 };
 
 struct BwdArgs {
@@ -49,11 +47,6 @@ struct BwdArgs {
 cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, int n_items,
                        cudaStream_t stream);
-
-// Merges split query tiles' partial outputs (a.part_o / a.part_lse) into
-// a.o and a.lse.
-cudaError_t launch_fwd_combine(int head_dim, const CombItem* items, int n_comb, const FwdArgs& a,
-                               cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(int head_dim, const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                   float* D, float* dq_acc, int64_t total_q, int hq,

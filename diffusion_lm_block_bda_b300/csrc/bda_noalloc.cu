@@ -106,7 +106,7 @@ bda_status bda_attn_fwd_noalloc(const bda_problem* prob, const bda_mask_desc* ma
                                 const void* k, const void* v, void* o, float* lse,
                                 bda_stream_t stream) {
   Shape s;
-  bda_status st = validate(prob, mask, &s, /*allow_split=*/false);  // no room for split outputs
+  bda_status st = validate(prob, mask, &s);
   if (st != BDA_OK) return st;
   const size_t need = plan_bytes(s);
   if (need > kNoAllocScratchBytes) return BDA_ERR_WORKSPACE;  // beyond the fixed 1 MiB

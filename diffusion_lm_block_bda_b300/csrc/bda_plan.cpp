@@ -36,53 +36,9 @@ int seq_prefix(const bda_mask_desc* m, int s, int lk) {
   return m->kind == BDA_MASK_STAIRCASE ? m->prefix_len_host[s] : lk;
 }
 
-// The forward item of the query tile starting at local token t0 of sequence
-// sq: the key tiles its rows see, FULL ones first.
-FwdItem fwd_item(const bda_problem* p, const bda_mask_desc* m, const Shape& s, int sq, int t0) {
-  const int q0 = p->cu_seqlens_q_host[sq], lq = p->cu_seqlens_q_host[sq + 1] - q0;
-  const int k0 = p->cu_seqlens_k_host[sq], lk = p->cu_seqlens_k_host[sq + 1] - k0;
-  const int P = seq_prefix(m, sq, lk);
-  const int B = s.B;
-  FwdItem it{};
-  it.q_row = q0 + t0;
-  it.q_len = std::min(s.tok, lq - t0);
-  it.pos0 = t0 + (lk - lq);
-  it.k_row = k0;
-  it.lk = lk;
-  it.prefix = P;
-  it.seq = sq;
-  it.part = -1;
-  const int p_lo = it.pos0, p_hi = it.pos0 + it.q_len - 1;
-  // [0, a(p)) grows with p: tiles inside [0, a(p_lo)) are FULL for every row.
-  const RowKeys lo = row_keys(p_lo, P, B, lk), hi = row_keys(p_hi, P, B, lk);
-  it.n_full = lo.a / kTileN;
-  it.r1_end = ceil_div(hi.a, kTileN);
-  it.r2_begin = it.r2_end = 0;
-  if (p_hi >= P) {  // copy rows: their own copies span [b(first copy row), e(p_hi))
-    const RowKeys c = row_keys(std::max(p_lo, P), P, B, lk);
-    int b0 = c.b / kTileN, b1 = ceil_div(hi.e, kTileN);
-    if (b0 <= it.r1_end) {
-      it.r1_end = std::max(it.r1_end, b1);
-    } else {
-      it.r2_begin = b0;
-      it.r2_end = b1;
-    }
-  }
-  it.work = it.r1_end + (it.r2_end - it.r2_begin);
-  return it;
-}
-
-// Splits of a query tile whose item is `it`, when `want` splits per tile are
-// wanted: cuts fall inside the FULL tiles only, and the last split keeps at
-// least one of them, so every row sees some key in every split.
-int splits_of(const FwdItem& it, int want) {
-  const int n = std::min(std::min(it.n_full, want), kMaxSplits);
-  return n >= 2 ? n : 1;
-}
-
 }  // namespace
 
-bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s, bool allow_split) {
+bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s) {
   if (!p || !m || !s) return BDA_ERR_INVALID_ARG;
   if (p->nseq < 0 || p->hq <= 0 || p->hkv <= 0 || p->head_dim <= 0) return BDA_ERR_INVALID_ARG;
   if (p->hq % p->hkv != 0) return BDA_ERR_INVALID_ARG;
@@ -135,51 +91,23 @@ bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s, bool
     if (nf >= (int64_t(1) << 30) / r.hq || nb >= (int64_t(1) << 30)) return BDA_ERR_INVALID_ARG;
     r.n_fwd = int(nf);
     r.n_bwd = int(nb);
-    // Too few units to fill the GPU (a decode step): split query tiles'
-    // key tiles across CTAs.
-    const int64_t units = nf * (r.hq / r.hg);
-    if (allow_split && units > 0 && 2 * units <= kSplitTargetUnits) {
-      r.split = int(kSplitTargetUnits / units);
-      for (int i = 0; i < p->nseq; ++i) {
-        const int lq = cq[i + 1] - cq[i];
-        for (int t0 = 0; t0 < lq; t0 += r.tok) {
-          const int n = splits_of(fwd_item(p, m, r, i, t0), r.split);
-          if (n > 1) {
-            r.n_comb += 1;
-            r.n_parts += n;
-            r.n_fwd += n - 1;
-          }
-        }
-      }
-      if (r.n_comb == 0) r.split = 0;
-    }
   }
   *s = r;
   return BDA_OK;
 }
 
-size_t plan_offset_comb(const Shape& s) {
+size_t plan_bytes(const Shape& s) {
   return kHeaderBytes + sizeof(FwdItem) * size_t(s.n_fwd) + sizeof(BwdItem) * size_t(s.n_bwd);
 }
 
-size_t plan_bytes(const Shape& s) {
-  return plan_offset_comb(s) + sizeof(CombItem) * size_t(s.n_comb);
-}
-
-size_t ws_offset_parts(const Shape& s) { return align256(plan_bytes(s)); }
-
-size_t ws_offset_D(const Shape& s) {
-  // split outputs: O fp32 [part][group][d][128 rows], then LSE fp32 [part][group][128]
-  const size_t rows = size_t(s.n_parts) * size_t(s.hq / s.hg) * size_t(kTileM);
-  return ws_offset_parts(s) + align256(sizeof(float) * rows * size_t(s.d + 1));
-}
+size_t ws_offset_D(const Shape& s) { return align256(plan_bytes(s)); }
 
 size_t ws_offset_dqacc(const Shape& s) {
   return ws_offset_D(s) + align256(sizeof(float) * size_t(s.hq) * size_t(s.total_q));
 }
 
 size_t workspace_bytes(const Shape& s, bool with_bwd) {
-  if (!with_bwd) return ws_offset_D(s);
+  if (!with_bwd) return align256(plan_bytes(s));
   return ws_offset_dqacc(s) +
          align256(sizeof(float) * size_t(s.total_q) * size_t(s.hq) * size_t(s.d));
 }
@@ -195,11 +123,7 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
   h->tok = s.tok;
   h->total_q = int32_t(s.total_q);
   h->total_k = int32_t(s.total_k);
-  h->n_comb = s.n_comb;
-  h->n_parts = s.n_parts;
   std::vector<FwdItem> fw;
-  std::vector<CombItem> comb;
-  int n_parts = 0;
   std::vector<BwdItem> bw;
   fw.reserve(s.n_fwd);
   bw.reserve(s.n_bwd);
@@ -209,36 +133,34 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
     const int k0 = p->cu_seqlens_k_host[sq], lk = p->cu_seqlens_k_host[sq + 1] - k0;
     const int P = seq_prefix(m, sq, lk);
     const int delta = lk - lq;
-    // forward: query tiles of tok tokens, each one item or s.split-wise split
+    // forward: query tiles of tok tokens
     for (int t0 = 0; t0 < lq; t0 += s.tok) {
-      const FwdItem it = fwd_item(p, m, s, sq, t0);
-      const int n = s.split > 0 ? splits_of(it, s.split) : 1;
-      if (n == 1) {
-        fw.push_back(it);
-        continue;
-      }
-      // Cuts b_j = min(floor(j T / n), n_full - n + j): strictly increasing,
-      // all below n_full, so splits 0..n-2 hold FULL tiles only.
-      const int T = it.work;
-      comb.push_back(CombItem{it.q_row, it.q_len, n_parts, n});
-      int b = 0;
-      for (int j = 0; j < n; ++j) {
-        const int e = j + 1 == n ? T : std::min((j + 1) * T / n, it.n_full - n + j + 1);
-        FwdItem x = it;
-        x.kt_off = b;
-        x.part = n_parts + j;
-        if (j + 1 < n) {
-          x.n_full = x.r1_end = e - b;
-          x.r2_begin = x.r2_end = 0;
+      FwdItem it{};
+      it.q_row = q0 + t0;
+      it.q_len = std::min(s.tok, lq - t0);
+      it.pos0 = t0 + delta;
+      it.k_row = k0;
+      it.lk = lk;
+      it.prefix = P;
+      it.seq = sq;
+      const int p_lo = it.pos0, p_hi = it.pos0 + it.q_len - 1;
+      // [0, a(p)) grows with p: tiles inside [0, a(p_lo)) are FULL for every row.
+      const RowKeys lo = row_keys(p_lo, P, B, lk), hi = row_keys(p_hi, P, B, lk);
+      it.n_full = lo.a / kTileN;
+      it.r1_end = ceil_div(hi.a, kTileN);
+      it.r2_begin = it.r2_end = 0;
+      if (p_hi >= P) {  // copy rows: their own copies span [b(first copy row), e(p_hi))
+        const RowKeys c = row_keys(std::max(p_lo, P), P, B, lk);
+        int b0 = c.b / kTileN, b1 = ceil_div(hi.e, kTileN);
+        if (b0 <= it.r1_end) {
+          it.r1_end = std::max(it.r1_end, b1);
         } else {
-          x.n_full = it.n_full - b;
-          x.r1_end = it.r1_end - b;
+          it.r2_begin = b0;
+          it.r2_end = b1;
         }
-        x.work = x.r1_end + (x.r2_end - x.r2_begin);
-        fw.push_back(x);
-        b = e;
       }
-      n_parts += n;
+      it.work = it.r1_end + (it.r2_end - it.r2_begin);
+      fw.push_back(it);
     }
     // backward: key tiles of 128 keys
     for (int kp = 0; kp < lk; kp += kTileN) {
@@ -280,7 +202,6 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
   std::memcpy(out + kHeaderBytes, fw.data(), sizeof(FwdItem) * fw.size());
   std::memcpy(out + kHeaderBytes + sizeof(FwdItem) * fw.size(), bw.data(),
               sizeof(BwdItem) * bw.size());
-  std::memcpy(out + plan_offset_comb(s), comb.data(), sizeof(CombItem) * comb.size());
 }
 
 long long count_pairs(const bda_problem* p, const bda_mask_desc* m, const Shape& s) {

@@ -21,8 +21,7 @@ from diffusion_lm_block_bda_b300 import Problem, workloads as W
 HDR = 256
 ITEM_INTS = 16
 FWD_FIELDS = ["q_row", "q_len", "pos0", "k_row", "lk", "prefix", "n_full", "r1_end", "r2_begin",
-              "r2_end", "work", "seq", "kt_off", "part"]
-COMB_FIELDS = ["q_row", "q_len", "part0", "n_part"]
+              "r2_end", "work", "seq"]
 BWD_FIELDS = ["k_row", "k_len", "kpos0", "q_row", "lq", "lk", "prefix", "q_begin", "q_end",
               "work", "seq"]
 
@@ -34,26 +33,19 @@ def decode(pb):
     hdr = a[:HDR // 4]
     magic, n_fwd, n_bwd, hg, tok = int(hdr[1]) & 0xffffffff, int(hdr[2]), int(hdr[3]), int(hdr[4]), int(hdr[5])
     assert magic == 0x42444131
-    n_comb, n_parts = int(hdr[8]), int(hdr[9])
-    n_items = n_fwd + n_bwd
-    items = a[HDR // 4:HDR // 4 + n_items * ITEM_INTS].reshape(-1, ITEM_INTS)
+    items = a[HDR // 4:].reshape(-1, ITEM_INTS)
     fw = [dict(zip(FWD_FIELDS, map(int, r))) for r in items[:n_fwd]]
-    bw = [dict(zip(BWD_FIELDS, map(int, r))) for r in items[n_fwd:n_items]]
-    comb = a[HDR // 4 + n_items * ITEM_INTS:].reshape(-1, 4)
-    assert comb.shape[0] == n_comb
-    comb = [dict(zip(COMB_FIELDS, map(int, r))) for r in comb]
-    assert sum(c["n_part"] for c in comb) == n_parts
-    return fw, bw, hg, tok, comb
+    bw = [dict(zip(BWD_FIELDS, map(int, r))) for r in items[n_fwd:n_fwd + n_bwd]]
+    return fw, bw, hg, tok
 
 
 def key_tiles(it):
-    return ([it["kt_off"] + n for n in range(it["r1_end"])] +
-            list(range(it["r2_begin"], it["r2_end"])))
+    return list(range(it["r1_end"])) + list(range(it["r2_begin"], it["r2_end"]))
 
 
 def check_plan(w):
     pb = Problem.from_workload(w)
-    fw, bw, hg, tok, comb = decode(pb)
+    fw, bw, hg, tok = decode(pb)
     G = w.hq // w.hkv
     assert G % hg == 0 and hg * tok == 128
     cq, ck = w.cu_seqlens_q, w.cu_seqlens_k
@@ -62,45 +54,28 @@ def check_plan(w):
         lq, lk = cq[s + 1] - cq[s], ck[s + 1] - ck[s]
         P = w.prefix[s] if w.kind == W.STAIRCASE else lk
         masks.append(oracle.mask(w.kind, w.block_size, P, lq, lk) if lq and lk else None)
-    # forward coverage: the items of one query tile (several when its key
-    # tiles are split) visit every key tile holding an allowed pair exactly
-    # once, FULL ones first; every row sees some key in every split
-    by_tile = {}
+    # forward coverage
+    seen_tiles = {}
     for it in fw:
         s = it["seq"]
+        M = masks[s]
         t0 = it["q_row"] - cq[s]
+        rows = M[t0:t0 + it["q_len"]]
         assert it["q_len"] == min(tok, (cq[s + 1] - cq[s]) - t0)
-        by_tile.setdefault((s, t0), []).append(it)
+        tiles = key_tiles(it)
+        assert len(tiles) == len(set(tiles)) == it["work"]
+        covered = np.zeros_like(rows)
+        for n, kt in enumerate(tiles):
+            blk = rows[:, kt * 128:(kt + 1) * 128]
+            assert blk.any(), ("empty tile scheduled", s, t0, kt)
+            if n < it["n_full"]:
+                assert blk.all() and blk.shape[1] == 128, ("FULL tile not full", s, t0, kt)
+            covered[:, kt * 128:(kt + 1) * 128] = True
+        assert not (rows & ~covered).any(), ("allowed pair not covered", s, t0)
+        seen_tiles[(s, t0)] = True
     for s in range(w.nseq):
         lq = cq[s + 1] - cq[s]
-        assert sorted(t0 for (s2, t0) in by_tile if s2 == s) == list(range(0, lq, tok))
-    comb_of = {c["q_row"]: c for c in comb}
-    for (s, t0), its in by_tile.items():
-        rows = masks[s][t0:t0 + its[0]["q_len"]]
-        covered = np.zeros_like(rows)
-        seen = []
-        for it in its:
-            tiles = key_tiles(it)
-            assert len(tiles) == it["work"] >= 1
-            seen += tiles
-            vis = np.zeros_like(rows)
-            for n, kt in enumerate(tiles):
-                blk = rows[:, kt * 128:(kt + 1) * 128]
-                assert blk.any(), ("empty tile scheduled", s, t0, kt)
-                if n < it["n_full"]:
-                    assert blk.all() and blk.shape[1] == 128, ("FULL tile not full", s, t0, kt)
-                covered[:, kt * 128:(kt + 1) * 128] = True
-                vis[:, kt * 128:(kt + 1) * 128] = rows[:, kt * 128:(kt + 1) * 128]
-            if len(its) > 1:
-                assert it["n_full"] >= 1 and vis.any(axis=1).all(), ("row without keys in a split", s, t0)
-        assert len(seen) == len(set(seen)), ("key tile visited twice", s, t0)
-        assert not (rows & ~covered).any(), ("allowed pair not covered", s, t0)
-        if len(its) == 1:
-            assert its[0]["part"] == -1 and its[0]["kt_off"] == 0
-        else:
-            c = comb_of[its[0]["q_row"]]
-            assert (c["q_len"], c["n_part"]) == (its[0]["q_len"], len(its))
-            assert sorted(it["part"] for it in its) == list(range(c["part0"], c["part0"] + len(its)))
+        assert all((s, t0) in seen_tiles for t0 in range(0, lq, tok))
     # backward coverage
     for it in bw:
         s = it["seq"]
@@ -181,18 +156,12 @@ def test_planner_named_workloads(name):
         copy_items = [it for it in fw if it["pos0"] >= 1024]
         assert copy_items and all(it["n_full"] == 8 and it["work"] == 9 for it in copy_items)
     if name == "c2":
-        # 8 units fill 8 of 148 SMs: the query tile's 17 key tiles (16 FULL)
-        # are split 16 ways, the last split keeping a FULL tile and the
-        # partial one
-        assert len(fw) == 16 and sum(it["work"] for it in fw) == 17
-        last = max(fw, key=lambda it: it["kt_off"])
-        assert (last["kt_off"], last["work"], last["n_full"]) == (15, 2, 1)
-        assert sorted(it["part"] for it in fw) == list(range(16))
+        assert len(fw) == 1 and fw[0]["work"] == 17 and fw[0]["n_full"] == 16
 
 
 def test_planner_long_sequence_counts():
     w = W.named("c5")
-    fw, bw, hg, tok, _ = decode(Problem.from_workload(w))
+    fw, bw, hg, tok = decode(Problem.from_workload(w))
     assert hg == 4 and tok == 32
     assert len(fw) == 32768 // 32 and len(bw) == 32768 // 128
     works = sorted(it["work"] for it in fw)
