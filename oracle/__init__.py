@@ -6,6 +6,8 @@ binding never do.  It shares no code with the CUDA path.
 
 `oracle.c` holds the plain definition (explicit mask, dense rows, fp64); this
 module marshals numpy/torch inputs into it, one packed sequence at a time.
+The `*_multi` functions cover the multi-block staircase (several active
+blocks per trajectory, each with its own group of copies).
 `brute.py` holds an independent NumPy brute force for tiny inputs.
 
 Mask kinds follow the ORL announcement thread (24vids.com mirror),
@@ -50,6 +52,19 @@ def _load():
         lib.oracle_bwd_seq.argtypes = ([c_int] * 8 + [c_dbl, pd, pd, pd, pd, c_int, c_int, pi,
                                                      c_int, pi, c_int, pd, pd, pd])
         lib.oracle_bwd_seq.restype = None
+        grp = [c_int, c_int, c_int, pi, pi, c_int]  # B, P, n_groups, copies, visible, L
+        lib.oracle_allowed_multi.argtypes = grp + [c_int, c_int]
+        lib.oracle_allowed_multi.restype = c_int
+        lib.oracle_mask_multi.argtypes = grp + [ctypes.POINTER(ctypes.c_uint8)]
+        lib.oracle_mask_multi.restype = None
+        lib.oracle_count_pairs_multi.argtypes = grp
+        lib.oracle_count_pairs_multi.restype = ctypes.c_longlong
+        lib.oracle_fwd_seq_multi.argtypes = grp + [c_int, c_int, c_int, c_dbl, pd, pd, pd, c_int,
+                                                   c_int, pi, c_int, pd, pd]
+        lib.oracle_fwd_seq_multi.restype = None
+        lib.oracle_bwd_seq_multi.argtypes = grp + [c_int, c_int, c_int, c_dbl, pd, pd, pd, pd,
+                                                   c_int, c_int, pi, c_int, pi, c_int, pd, pd, pd]
+        lib.oracle_bwd_seq_multi.restype = None
         _lib = lib
     return _lib
 
@@ -175,6 +190,76 @@ def bwd(kind, B, cu_q, cu_k, prefix, Q, K, V, dO, hq, hkv, scale, kv_heads=None)
         dQ[q0:q1] = dq
         dK[k0:k1] = dk
         dV[k0:k1] = dv
+    return dQ, dK, dV
+
+
+# ---------------------------------------------------- multi-block staircase
+# One trajectory (Lq = Lk = L): a clean prefix [0, P), block-causal in blocks
+# of B; then groups g = 0.. of copies[g] copies (B tokens each) of one active
+# block, whose copies see the clean keys [0, visible[g]) and themselves.
+# Requires sum(copies) * B == L - P and 0 <= visible[g] <= P.
+
+def _groups(B, P, copies, visible, L):
+    c = np.ascontiguousarray(np.asarray(copies, dtype=np.int32))
+    v = np.ascontiguousarray(np.asarray(visible, dtype=np.int32))
+    if c.shape != v.shape or c.ndim != 1:
+        raise ValueError("copies and visible: one entry per group")
+    if int(c.sum()) * B != L - P or (c < 0).any() or (v < 0).any() or (v > P).any():
+        raise ValueError("groups do not tile [P, L) or see past the prefix")
+    return (B, P, int(c.size), _ptr(c, ctypes.c_int32), _ptr(v, ctypes.c_int32), L), (c, v)
+
+
+def allowed_multi(B, P, copies, visible, L, i, j) -> bool:
+    g, keep = _groups(B, P, copies, visible, L)
+    return bool(_load().oracle_allowed_multi(*g, i, j))
+
+
+def mask_multi(B, P, copies, visible, L) -> np.ndarray:
+    g, keep = _groups(B, P, copies, visible, L)
+    m = np.zeros((L, L), dtype=np.uint8)
+    _load().oracle_mask_multi(*g, _ptr(m, ctypes.c_uint8))
+    return m.astype(bool)
+
+
+def count_pairs_multi(B, P, copies, visible, L) -> int:
+    g, keep = _groups(B, P, copies, visible, L)
+    return int(_load().oracle_count_pairs_multi(*g))
+
+
+def fwd_seq_multi(B, P, copies, visible, Q, K, V, hq, hkv, scale, heads=None, rows=None):
+    """fwd_seq for one multi-block staircase trajectory."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    L, d = Q.shape[0], Q.shape[2]
+    g, keep = _groups(B, P, copies, visible, L)
+    h_lo, h_hi = heads if heads is not None else (0, hq)
+    r, nr = _rows(rows)
+    n = L if r is None else nr
+    O = np.full((n, hq, d), np.nan)
+    LSE = np.full((hq, n), np.nan)
+    _load().oracle_fwd_seq_multi(*g, hq, hkv, d, scale, _ptr(Q), _ptr(K), _ptr(V), h_lo, h_hi,
+                                 None if r is None else _ptr(r, ctypes.c_int32), n, _ptr(O),
+                                 _ptr(LSE))
+    return O, LSE
+
+
+def bwd_seq_multi(B, P, copies, visible, Q, K, V, dO, hq, hkv, scale, kv_heads=None, qrows=None,
+                  krows=None):
+    """bwd_seq for one multi-block staircase trajectory."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    L, d = Q.shape[0], Q.shape[2]
+    g, keep = _groups(B, P, copies, visible, L)
+    lo, hi = kv_heads if kv_heads is not None else (0, hkv)
+    qr, nq = _rows(qrows)
+    kr, nk = _rows(krows)
+    nq = L if qr is None else nq
+    nk = L if kr is None else nk
+    dQ = np.full((nq, hq, d), np.nan)
+    dK = np.full((nk, hkv, d), np.nan)
+    dV = np.full((nk, hkv, d), np.nan)
+    _load().oracle_bwd_seq_multi(*g, hq, hkv, d, scale, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), lo,
+                                 hi, None if qr is None else _ptr(qr, ctypes.c_int32), nq,
+                                 None if kr is None else _ptr(kr, ctypes.c_int32), nk, _ptr(dQ),
+                                 _ptr(dK), _ptr(dV))
     return dQ, dK, dV
 
 

@@ -49,6 +49,25 @@ def mask_staircase(L, B, P):
     return M
 
 
+def mask_staircase_multi(L, B, P, copies, visible):
+    """Prefix of P tokens, block-causal inside itself; then, group after
+    group, copies[g] copies of B tokens, each seeing the clean keys
+    [0, visible[g]) and itself."""
+    M = np.zeros((L, L), dtype=bool)
+    pb = blocks(P, B)
+    for b, (s, e) in enumerate(pb):
+        for (s2, e2) in pb[: b + 1]:
+            M[s:e, s2:e2] = True
+    s = P
+    for n, vis in zip(copies, visible):
+        for _ in range(n):
+            M[s:s + B, :vis] = True
+            M[s:s + B, s:s + B] = True
+            s += B
+    assert s == L
+    return M
+
+
 def attention(Q, K, V, M, scale, hkv):
     """Q [Lq][Hq][d], K/V [Lk][Hkv][d], M [Lq][Lk] bool.  fp64 dense.
     Returns O [Lq][Hq][d], LSE [Hq][Lq], P [Hq][Lq][Lk]."""

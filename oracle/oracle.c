@@ -28,7 +28,12 @@
  *   - when a sequence has fewer queries than keys (a decode step), query row i
  *     sits at key position p = i + (Lk - Lq) (aligned to the end);
  *   - GQA: query head h reads KV head floor(h / G), G = Hq / Hkv;
- *   - LSE is the natural logarithm.
+ *   - LSE is the natural logarithm;
+ *   - several active blocks per trajectory (the announcement thread's
+ *     "irregular trajectories", Insight 3): the copies of each active block
+ *     form a group after the prefix, and a group's copies see the clean keys
+ *     before their block's position (the prompt and the clean blocks before
+ *     it) and themselves only -- the multi-block staircase below.
  *
  * Layout of every array handed in (one sequence at a time, row-major fp64):
  *   Q, dO, O, dQ : [Lq][Hq][d]     K, V, dK, dV : [Lk][Hkv][d]
@@ -47,6 +52,21 @@
 
 #define ORACLE_BLOCK_CAUSAL 0
 #define ORACLE_STAIRCASE 1
+#define ORACLE_STAIRCASE_MULTI 2
+
+/* A sequence's mask.  The multi-block staircase (several active blocks per
+ * trajectory, the "irregular trajectories" of the announcement thread,
+ * Insight 3) generalises the staircase: after the clean prefix [0, P) come
+ * n_groups groups of copies; group g holds copies[g] copies of one active
+ * block (B tokens each), and its copies see the clean keys [0, visible[g])
+ * -- the prompt and the clean blocks before that active block -- and their
+ * own copy only.  The staircase is one group with visible[0] = P. */
+typedef struct {
+    int kind, B, P;
+    int n_groups;
+    const int32_t *copies;
+    const int32_t *visible;
+} oracle_mask_t;
 
 /* allowed(i, j): may local query row i attend to local key j?
  * Block-causal (announcement thread, highlight 3):
@@ -54,32 +74,98 @@
  * Staircase (announcement thread, Insight 3; paper card, Figure 3):
  *     row in the prefix (p < P):  j < P  and  floor(j / B) <= floor(p / B)
  *     row in copy c = floor((p - P) / B):  j < P  or  floor((j - P) / B) == c */
-int oracle_allowed(int kind, int B, int P, int Lq, int Lk, int i, int j)
+static int allowed_m(const oracle_mask_t *mk, int Lq, int Lk, int i, int j)
 {
+    const int B = mk->B, P = mk->P;
     if (i < 0 || i >= Lq || j < 0 || j >= Lk || B <= 0) return 0;
     long p = (long)i + (long)(Lk - Lq);
-    if (kind == ORACLE_BLOCK_CAUSAL) return (j / B) <= (p / B);
+    if (mk->kind == ORACLE_BLOCK_CAUSAL) return (j / B) <= (p / B);
     if (p < P) return j < P && (j / B) <= (p / B);
-    if (j < P) return 1;
-    return ((long)j - P) / B == (p - P) / B;
+    if (mk->kind == ORACLE_STAIRCASE) {
+        if (j < P) return 1;
+        return ((long)j - P) / B == (p - P) / B;
+    }
+    /* multi-block staircase: find the row's group, then its own copy */
+    long start = P;
+    for (int g = 0; g < mk->n_groups; ++g) {
+        const long span = (long)mk->copies[g] * B;
+        if (p < start + span) {
+            const long c0 = start + ((p - start) / B) * B;
+            return j < mk->visible[g] || (j >= c0 && j < c0 + B);
+        }
+        start += span;
+    }
+    return 0;
+}
+
+static oracle_mask_t simple_mask(int kind, int B, int P)
+{
+    oracle_mask_t mk = {kind, B, P, 0, NULL, NULL};
+    return mk;
+}
+
+static oracle_mask_t multi_mask(int B, int P, int n_groups, const int32_t *copies,
+                                const int32_t *visible)
+{
+    oracle_mask_t mk = {ORACLE_STAIRCASE_MULTI, B, P, n_groups, copies, visible};
+    return mk;
+}
+
+int oracle_allowed(int kind, int B, int P, int Lq, int Lk, int i, int j)
+{
+    const oracle_mask_t mk = simple_mask(kind, B, P);
+    return allowed_m(&mk, Lq, Lk, i, j);
+}
+
+int oracle_allowed_multi(int B, int P, int n_groups, const int32_t *copies,
+                         const int32_t *visible, int L, int i, int j)
+{
+    const oracle_mask_t mk = multi_mask(B, P, n_groups, copies, visible);
+    return allowed_m(&mk, L, L, i, j);
+}
+
+static void mask_m(const oracle_mask_t *mk, int Lq, int Lk, uint8_t *M)
+{
+    for (int i = 0; i < Lq; ++i)
+        for (int j = 0; j < Lk; ++j)
+            M[(size_t)i * Lk + j] = (uint8_t)allowed_m(mk, Lq, Lk, i, j);
 }
 
 /* The explicit mask of one sequence, M[i*Lk + j] in {0,1}. */
 void oracle_mask(int kind, int B, int P, int Lq, int Lk, uint8_t *M)
 {
+    const oracle_mask_t mk = simple_mask(kind, B, P);
+    mask_m(&mk, Lq, Lk, M);
+}
+
+void oracle_mask_multi(int B, int P, int n_groups, const int32_t *copies, const int32_t *visible,
+                       int L, uint8_t *M)
+{
+    const oracle_mask_t mk = multi_mask(B, P, n_groups, copies, visible);
+    mask_m(&mk, L, L, M);
+}
+
+static long long count_pairs_m(const oracle_mask_t *mk, int Lq, int Lk)
+{
+    long long n = 0;
     for (int i = 0; i < Lq; ++i)
         for (int j = 0; j < Lk; ++j)
-            M[(size_t)i * Lk + j] = (uint8_t)oracle_allowed(kind, B, P, Lq, Lk, i, j);
+            n += allowed_m(mk, Lq, Lk, i, j);
+    return n;
 }
 
 /* Number of allowed (i, j) pairs of one sequence (per head). */
 long long oracle_count_pairs(int kind, int B, int P, int Lq, int Lk)
 {
-    long long n = 0;
-    for (int i = 0; i < Lq; ++i)
-        for (int j = 0; j < Lk; ++j)
-            n += oracle_allowed(kind, B, P, Lq, Lk, i, j);
-    return n;
+    const oracle_mask_t mk = simple_mask(kind, B, P);
+    return count_pairs_m(&mk, Lq, Lk);
+}
+
+long long oracle_count_pairs_multi(int B, int P, int n_groups, const int32_t *copies,
+                                   const int32_t *visible, int L)
+{
+    const oracle_mask_t mk = multi_mask(B, P, n_groups, copies, visible);
+    return count_pairs_m(&mk, L, L);
 }
 
 static int max_threads(void)
@@ -95,14 +181,14 @@ int oracle_num_threads(void) { return max_threads(); }
 
 /* One query row of one head: fill mrow (mask row), S (scores, -inf where
  * masked), P (probabilities), and return LSE.  O row (d values) written. */
-static double row_forward(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int d,
+static double row_forward(const oracle_mask_t *mk, int Lq, int Lk, int Hq, int Hkv, int d,
                           double scale, const double *Q, const double *K, const double *V,
                           int h, int i, uint8_t *mrow, double *S, double *Pr, double *Orow)
 {
     const int G = Hq / Hkv;
     const int kvh = h / G;
     const double *q = Q + ((size_t)i * Hq + h) * d;
-    for (int j = 0; j < Lk; ++j) mrow[j] = (uint8_t)oracle_allowed(kind, B, P, Lq, Lk, i, j);
+    for (int j = 0; j < Lk; ++j) mrow[j] = (uint8_t)allowed_m(mk, Lq, Lk, i, j);
     /* S_ij = scale * <Q_i, K_j>, -inf where not allowed */
     double m = -INFINITY;
     for (int j = 0; j < Lk; ++j) {
@@ -133,9 +219,9 @@ static double row_forward(int kind, int B, int P, int Lq, int Lk, int Hq, int Hk
 /* Forward for one sequence, query heads [h_lo, h_hi).  rows == NULL: every
  * row, outputs indexed by row; else only rows[0..nrows), outputs indexed by
  * position in that list (O: [nrows][Hq][d], LSE: [Hq][nrows]). */
-void oracle_fwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int d, double scale,
-                    const double *Q, const double *K, const double *V, int h_lo, int h_hi,
-                    const int32_t *rows, int nrows, double *O, double *LSE)
+static void fwd_seq_m(const oracle_mask_t *mk, int Lq, int Lk, int Hq, int Hkv, int d,
+                      double scale, const double *Q, const double *K, const double *V, int h_lo,
+                      int h_hi, const int32_t *rows, int nrows, double *O, double *LSE)
 {
     const int nr = rows ? nrows : Lq;
     const long ntask = (long)(h_hi - h_lo) * nr;
@@ -150,13 +236,30 @@ void oracle_fwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int
             const int r = (int)(t % nr);
             const int i = rows ? rows[r] : r;
             double *Orow = O + ((size_t)r * Hq + h) * d;
-            LSE[(size_t)h * nr + r] = row_forward(kind, B, P, Lq, Lk, Hq, Hkv, d, scale, Q, K, V,
-                                                  h, i, mrow, S, Pr, Orow);
+            LSE[(size_t)h * nr + r] = row_forward(mk, Lq, Lk, Hq, Hkv, d, scale, Q, K, V, h, i,
+                                                  mrow, S, Pr, Orow);
         }
         free(mrow);
         free(S);
         free(Pr);
     }
+}
+
+void oracle_fwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int d, double scale,
+                    const double *Q, const double *K, const double *V, int h_lo, int h_hi,
+                    const int32_t *rows, int nrows, double *O, double *LSE)
+{
+    const oracle_mask_t mk = simple_mask(kind, B, P);
+    fwd_seq_m(&mk, Lq, Lk, Hq, Hkv, d, scale, Q, K, V, h_lo, h_hi, rows, nrows, O, LSE);
+}
+
+void oracle_fwd_seq_multi(int B, int P, int n_groups, const int32_t *copies,
+                          const int32_t *visible, int L, int Hq, int Hkv, int d, double scale,
+                          const double *Q, const double *K, const double *V, int h_lo, int h_hi,
+                          const int32_t *rows, int nrows, double *O, double *LSE)
+{
+    const oracle_mask_t mk = multi_mask(B, P, n_groups, copies, visible);
+    fwd_seq_m(&mk, L, L, Hq, Hkv, d, scale, Q, K, V, h_lo, h_hi, rows, nrows, O, LSE);
 }
 
 /* Backward for one sequence, KV heads [kvh_lo, kvh_hi) (and their G query
@@ -168,10 +271,10 @@ void oracle_fwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int
  * position in that list: [nq][Hq][d].  krows (or NULL = all Lk keys) selects
  * the dK/dV rows computed: [nk][Hkv][d].  Only heads in range are written.
  * P_ij for a key column is exp(S_ij - LSE_i), the same softmax. */
-void oracle_bwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int d, double scale,
-                    const double *Q, const double *K, const double *V, const double *dO,
-                    int kvh_lo, int kvh_hi, const int32_t *qrows, int nq, const int32_t *krows,
-                    int nk, double *dQ, double *dK, double *dV)
+static void bwd_seq_m(const oracle_mask_t *mk, int Lq, int Lk, int Hq, int Hkv, int d,
+                      double scale, const double *Q, const double *K, const double *V,
+                      const double *dO, int kvh_lo, int kvh_hi, const int32_t *qrows, int nq,
+                      const int32_t *krows, int nk, double *dQ, double *dK, double *dV)
 {
     const int G = Hq / Hkv;
     const int h_lo = kvh_lo * G, h_hi = kvh_hi * G;
@@ -186,7 +289,7 @@ void oracle_bwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int
     for (int i = 0; i < Lq; ++i) {
         if (need[i]) continue;
         for (int r = 0; r < nkr; ++r)
-            if (oracle_allowed(kind, B, P, Lq, Lk, i, krows ? krows[r] : r)) { need[i] = 1; break; }
+            if (allowed_m(mk, Lq, Lk, i, krows ? krows[r] : r)) { need[i] = 1; break; }
     }
     int32_t *qpos = (int32_t *)malloc(sizeof(int32_t) * ((size_t)Lq + 1));
     for (int i = 0; i < Lq; ++i) qpos[i] = -1;
@@ -211,8 +314,8 @@ void oracle_bwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int
             const int i = (int)(t % Lq);
             if (!need[i]) continue;
             const int kvh = h / G;
-            const double lse = row_forward(kind, B, P, Lq, Lk, Hq, Hkv, d, scale, Q, K, V, h, i,
-                                           mrow, S, Pr, Orow);
+            const double lse = row_forward(mk, Lq, Lk, Hq, Hkv, d, scale, Q, K, V, h, i, mrow, S,
+                                           Pr, Orow);
             const double *dout = dO + ((size_t)i * Hq + h) * d;
             double D = 0.0;
             for (int c = 0; c < d; ++c) D += dout[c] * Orow[c];
@@ -252,7 +355,7 @@ void oracle_bwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int
         const double *v = V + ((size_t)j * Hkv + kvh) * d;
         for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
             for (int i = 0; i < Lq; ++i) {
-                if (!oracle_allowed(kind, B, P, Lq, Lk, i, j)) continue;
+                if (!allowed_m(mk, Lq, Lk, i, j)) continue;
                 const double *q = Q + ((size_t)i * Hq + h) * d;
                 const double *dout = dO + ((size_t)i * Hq + h) * d;
                 double s = 0.0, dp = 0.0;
@@ -270,4 +373,25 @@ void oracle_bwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int
     free(qpos);
     free(LSE);
     free(Dv);
+}
+
+void oracle_bwd_seq(int kind, int B, int P, int Lq, int Lk, int Hq, int Hkv, int d, double scale,
+                    const double *Q, const double *K, const double *V, const double *dO,
+                    int kvh_lo, int kvh_hi, const int32_t *qrows, int nq, const int32_t *krows,
+                    int nk, double *dQ, double *dK, double *dV)
+{
+    const oracle_mask_t mk = simple_mask(kind, B, P);
+    bwd_seq_m(&mk, Lq, Lk, Hq, Hkv, d, scale, Q, K, V, dO, kvh_lo, kvh_hi, qrows, nq, krows, nk,
+              dQ, dK, dV);
+}
+
+void oracle_bwd_seq_multi(int B, int P, int n_groups, const int32_t *copies,
+                          const int32_t *visible, int L, int Hq, int Hkv, int d, double scale,
+                          const double *Q, const double *K, const double *V, const double *dO,
+                          int kvh_lo, int kvh_hi, const int32_t *qrows, int nq,
+                          const int32_t *krows, int nk, double *dQ, double *dK, double *dV)
+{
+    const oracle_mask_t mk = multi_mask(B, P, n_groups, copies, visible);
+    bwd_seq_m(&mk, L, L, Hq, Hkv, d, scale, Q, K, V, dO, kvh_lo, kvh_hi, qrows, nq, krows, nk, dQ,
+              dK, dV);
 }
