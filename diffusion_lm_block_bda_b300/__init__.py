@@ -28,6 +28,7 @@ BDA_ERR_DEVICE_TIMEOUT = 5
 
 BDA_MASK_BLOCK_CAUSAL = 0
 BDA_MASK_STAIRCASE = 1
+BDA_MASK_STAIRCASE_MULTI = 2
 
 EXPORTED = (
     "bda_attn_plan_size", "bda_attn_workspace_size", "bda_attn_plan", "bda_attn_plan_host",
@@ -40,7 +41,10 @@ EXPORTED = (
 
 class BdaMaskDesc(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("prefix_len_host", ctypes.POINTER(ctypes.c_int32))]
+                ("prefix_len_host", ctypes.POINTER(ctypes.c_int32)),
+                ("group_offsets_host", ctypes.POINTER(ctypes.c_int32)),
+                ("group_copies_host", ctypes.POINTER(ctypes.c_int32)),
+                ("group_visible_host", ctypes.POINTER(ctypes.c_int32))]
 
 
 class BdaProblem(ctypes.Structure):
@@ -130,7 +134,9 @@ class Problem:
     """Host-side problem + mask description (keeps the ctypes arrays alive)."""
 
     def __init__(self, cu_seqlens_q, cu_seqlens_k, hq, hkv, head_dim, kind, block_size,
-                 prefix_len=None, softmax_scale=0.0):
+                 prefix_len=None, softmax_scale=0.0, groups=None):
+        """groups (BDA_MASK_STAIRCASE_MULTI): per sequence a list of
+        (copies, visible) pairs, one per active block, in order."""
         self.cu_q = [int(x) for x in cu_seqlens_q]
         self.cu_k = [int(x) for x in cu_seqlens_k]
         self.hq, self.hkv, self.head_dim = int(hq), int(hkv), int(head_dim)
@@ -138,10 +144,19 @@ class Problem:
         self.prefix_len = None if prefix_len is None else [int(x) for x in prefix_len]
         self._cq, self._ck = _i32(self.cu_q), _i32(self.cu_k)
         self._pf = _i32(self.prefix_len) if self.prefix_len is not None else None
+        self.groups = None if groups is None else [[(int(c), int(v)) for c, v in g] for g in groups]
+        self._go = self._gc = self._gv = None
+        if self.groups is not None:
+            offs = [0]
+            for g in self.groups:
+                offs.append(offs[-1] + len(g))
+            self._go = _i32(offs)
+            self._gc = _i32([c for g in self.groups for c, _ in g] or [0])
+            self._gv = _i32([v for g in self.groups for _, v in g] or [0])
         self.prob = BdaProblem(len(self.cu_q) - 1, self.hq, self.hkv, self.head_dim,
                                float(softmax_scale or 0.0), self._cq, self._ck)
-        self.mask = BdaMaskDesc(self.kind, self.block_size,
-                                self._pf if self._pf is not None else None)
+        self.mask = BdaMaskDesc(self.kind, self.block_size, self._pf, self._go, self._gc,
+                                self._gv)
 
     @property
     def total_q(self):

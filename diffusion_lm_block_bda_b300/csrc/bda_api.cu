@@ -114,7 +114,7 @@ size_t bda_attn_workspace_size(const bda_problem* prob, const bda_mask_desc* mas
 
 long long bda_attn_count_pairs(const bda_problem* prob, const bda_mask_desc* mask) {
   Shape s;
-  if (validate(prob, mask, &s) != BDA_OK) return -1;
+  if (validate(prob, mask, &s, /*count_only=*/true) != BDA_OK) return -1;
   return count_pairs(prob, mask, s);
 }
 

@@ -22,7 +22,10 @@ struct Shape {
 };
 
 // Validates the problem and mask; fills `s`.  Host-only, launches nothing.
-bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s);
+// A valid multi-block staircase gives BDA_ERR_UNSUPPORTED (no kernel takes it
+// yet) unless count_only, for which it is BDA_OK.
+bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s,
+                    bool count_only = false);
 
 size_t plan_bytes(const Shape& s);
 size_t workspace_bytes(const Shape& s, bool with_bwd);

@@ -38,17 +38,23 @@ int seq_prefix(const bda_mask_desc* m, int s, int lk) {
 
 }  // namespace
 
-bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s) {
+bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s, bool count_only) {
   if (!p || !m || !s) return BDA_ERR_INVALID_ARG;
   if (p->nseq < 0 || p->hq <= 0 || p->hkv <= 0 || p->head_dim <= 0) return BDA_ERR_INVALID_ARG;
   if (p->hq % p->hkv != 0) return BDA_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return BDA_ERR_UNSUPPORTED;
-  if (m->kind != BDA_MASK_BLOCK_CAUSAL && m->kind != BDA_MASK_STAIRCASE) return BDA_ERR_INVALID_ARG;
+  const bool multi = m->kind == BDA_MASK_STAIRCASE_MULTI;
+  if (m->kind != BDA_MASK_BLOCK_CAUSAL && m->kind != BDA_MASK_STAIRCASE && !multi)
+    return BDA_ERR_INVALID_ARG;
   if (m->block_size < 1) return BDA_ERR_INVALID_ARG;
   if (!(p->softmax_scale == p->softmax_scale) || std::isinf(p->softmax_scale))
     return BDA_ERR_INVALID_ARG;
   if (p->nseq > 0 && (!p->cu_seqlens_q_host || !p->cu_seqlens_k_host)) return BDA_ERR_INVALID_ARG;
-  if (p->nseq > 0 && m->kind == BDA_MASK_STAIRCASE && !m->prefix_len_host)
+  if (p->nseq > 0 && m->kind != BDA_MASK_BLOCK_CAUSAL && !m->prefix_len_host)
+    return BDA_ERR_INVALID_ARG;
+  if (p->nseq > 0 && multi &&
+      (!m->group_offsets_host || !m->group_copies_host || !m->group_visible_host ||
+       m->group_offsets_host[0] != 0))
     return BDA_ERR_INVALID_ARG;
   Shape r;
   r.nseq = p->nseq;
@@ -75,10 +81,22 @@ bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s) {
       if (lq > 0 && lk == 0) return BDA_ERR_INVALID_ARG;  // queries with nothing to see
       if (m->kind == BDA_MASK_BLOCK_CAUSAL) {
         if (lq > lk) return BDA_ERR_INVALID_ARG;  // early queries would see no key
-      } else {
+      } else if (!multi) {
         const int64_t P = m->prefix_len_host[i];
         if (lq != lk || P < 0 || P > lk || (lk - P) % m->block_size != 0)
           return BDA_ERR_INVALID_ARG;
+      } else {
+        // groups of copies tile [P, L) and see at most the prefix
+        const int64_t P = m->prefix_len_host[i];
+        const int32_t g0 = m->group_offsets_host[i], g1 = m->group_offsets_host[i + 1];
+        if (lq != lk || P < 0 || P > lk || g1 < g0) return BDA_ERR_INVALID_ARG;
+        int64_t tokens = 0;
+        for (int32_t g = g0; g < g1; ++g) {
+          const int64_t c = m->group_copies_host[g], v = m->group_visible_host[g];
+          if (c < 0 || v < 0 || v > P) return BDA_ERR_INVALID_ARG;
+          tokens += c * m->block_size;
+        }
+        if (tokens != lk - P) return BDA_ERR_INVALID_ARG;
       }
       nf += (lq + r.tok - 1) / r.tok;
       nb += (lk + kTileN - 1) / kTileN;
@@ -93,7 +111,8 @@ bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s) {
     r.n_bwd = int(nb);
   }
   *s = r;
-  return BDA_OK;
+  // The multi-block staircase is validated and counted; no kernel takes it yet.
+  return multi && !count_only ? BDA_ERR_UNSUPPORTED : BDA_OK;
 }
 
 size_t plan_bytes(const Shape& s) {
@@ -205,6 +224,18 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
 }
 
 long long count_pairs(const bda_problem* p, const bda_mask_desc* m, const Shape& s) {
+  if (m->kind == BDA_MASK_STAIRCASE_MULTI) {
+    // prefix rows: block-causal inside [0, P); a copy row: its group's
+    // visible clean keys and its own B-token copy
+    long long n = 0;
+    for (int sq = 0; sq < s.nseq; ++sq) {
+      const int P = m->prefix_len_host[sq];
+      for (int i = 0; i < P; ++i) n += std::min(P, (i / s.B + 1) * s.B);
+      for (int g = m->group_offsets_host[sq]; g < m->group_offsets_host[sq + 1]; ++g)
+        n += (long long)m->group_copies_host[g] * s.B * (m->group_visible_host[g] + s.B);
+    }
+    return n;
+  }
   long long n = 0;
   for (int sq = 0; sq < s.nseq; ++sq) {
     const int lq = p->cu_seqlens_q_host[sq + 1] - p->cu_seqlens_q_host[sq];

@@ -70,14 +70,34 @@ typedef enum {
   BDA_ERR_DEVICE_TIMEOUT = 5  /* a kernel's bounded wait ran out (reported after the fact) */
 } bda_status;
 
-typedef enum { BDA_MASK_BLOCK_CAUSAL = 0, BDA_MASK_STAIRCASE = 1 } bda_mask_kind;
+typedef enum {
+  BDA_MASK_BLOCK_CAUSAL = 0,
+  BDA_MASK_STAIRCASE = 1,
+  /* Several active blocks per trajectory (the "irregular trajectories" the
+   * announcement thread's Insight 3 replays with the staircase kernel):
+   * after the clean prefix [0, P) -- block-causal in blocks of B -- come
+   * groups of copies, one group per active block, in order; group g holds
+   * group_copies[g] copies of B tokens, and each of its copies sees the
+   * clean keys [0, group_visible[g]) (the prompt and the clean blocks before
+   * its block) and itself only.  STAIRCASE is one group with visible = P.
+   * Validated and counted (bda_attn_count_pairs); the compute calls return
+   * BDA_ERR_UNSUPPORTED for it in this version. */
+  BDA_MASK_STAIRCASE_MULTI = 2
+} bda_mask_kind;
 
 /* Mask descriptor.  The mask is never materialised: kernels evaluate it from
  * block indices (see the file comment for its definition). */
 typedef struct {
   int32_t kind;                   /* bda_mask_kind */
   int32_t block_size;             /* B >= 1; staircase copies are B tokens long */
-  const int32_t *prefix_len_host; /* staircase: [nseq] prefix lengths (host); NULL otherwise */
+  const int32_t *prefix_len_host; /* staircase kinds: [nseq] prefix lengths (host); else NULL */
+  /* STAIRCASE_MULTI only (else NULL): sequence s owns groups
+   * [group_offsets_host[s], group_offsets_host[s+1]) of group_copies_host /
+   * group_visible_host; sum of its copies * B == its length - P, and
+   * 0 <= visible <= P. */
+  const int32_t *group_offsets_host; /* [nseq+1], starts at 0, non-decreasing */
+  const int32_t *group_copies_host;  /* copies per group, >= 0 */
+  const int32_t *group_visible_host; /* clean keys each group's copies see */
 } bda_mask_desc;
 
 /* Problem shape.  softmax_scale <= 0 selects 1/sqrt(head_dim). */

@@ -149,3 +149,44 @@ def test_count_pairs_matches_oracle():
 def test_count_pairs_named_workloads():
     for name, want in (("c1", 36864), ("c2", 66560), ("c4", 8650752), ("c5", 537919488)):
         assert bda.bda_attn_count_pairs(Problem.from_workload(W.named(name))) == want
+
+
+# Multi-block staircase: described at the boundary, validated and counted on
+# the host; no kernel takes it yet, so every compute call reports
+# BDA_ERR_UNSUPPORTED before launching anything.
+MULTI = dict(kind=bda.BDA_MASK_STAIRCASE_MULTI, cu_seqlens_q=[0, 224, 576],
+             cu_seqlens_k=[0, 224, 576], prefix_len=[128, 64],
+             groups=[[(2, 64), (1, 128)], [(4, 32), (0, 0), (5, 64)]])
+
+
+def test_multi_block_staircase_is_counted_like_the_oracle_and_unsupported():
+    pb = _pb(**MULTI)
+    L = bda.lib()
+    want = 0
+    for s, g in enumerate(MULTI["groups"]):
+        n = MULTI["cu_seqlens_q"][s + 1] - MULTI["cu_seqlens_q"][s]
+        want += oracle.count_pairs_multi(32, MULTI["prefix_len"][s], [c for c, _ in g],
+                                         [v for _, v in g], n)
+    assert L.bda_attn_count_pairs(*pb.refs()) == want
+    assert L.bda_attn_plan_size(*pb.refs()) == 0
+    assert L.bda_attn_workspace_size(*pb.refs(), 1) == 0
+    buf = torch.zeros(1 << 16, dtype=torch.uint8)
+    assert L.bda_attn_plan_host(*pb.refs(), buf.data_ptr(), buf.numel()) == bda.BDA_ERR_UNSUPPORTED
+    assert _fwd_status(pb, ws_bytes=1 << 30) == bda.BDA_ERR_UNSUPPORTED
+    assert L.bda_attn_bwd(*pb.refs(), *[FAKE] * 9, FAKE, 1 << 30, None) == bda.BDA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw", [
+    dict(groups=[[(2, 64), (2, 128)], [(4, 32), (0, 0), (5, 64)]]),   # copies overrun L
+    dict(groups=[[(2, 64), (1, 129)], [(4, 32), (0, 0), (5, 64)]]),   # sees past the prefix
+    dict(groups=[[(3, 64), (0, 128)], [(4, 32), (0, 0), (5, -1)]]),   # negative visible
+    dict(groups=[[(2, 64), (1, 128)], [(-1, 32), (0, 0), (10, 64)]]),  # negative copies
+    dict(groups=None),                                                 # no group arrays
+    dict(cu_seqlens_k=[0, 224, 577]),                                  # Lq != Lk
+    dict(prefix_len=None),
+])
+def test_malformed_multi_block_staircase_rejected(kw):
+    pb = _pb(**{**MULTI, **kw})
+    L = bda.lib()
+    assert L.bda_attn_count_pairs(*pb.refs()) == -1
+    assert _fwd_status(pb, ws_bytes=1 << 30) == bda.BDA_ERR_INVALID_ARG
