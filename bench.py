@@ -275,7 +275,7 @@ def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
     host enqueues, so the events bracket GPU time only.  `us`: median time of
     the forward; `achieved` = the minimum bytes (Q, K, V read once, O and LSE
     written) / `us`.  `graph_us`: one copy's forward captured in a CUDA graph
-    and replayed back to back (everything in L2)."""
+    and replayed back to back (everything in L2), GPU time per replay."""
     from diffusion_lm_block_bda_b300 import Problem
     w = W.named("c2")
     pb = Problem.from_workload(w)
@@ -295,7 +295,7 @@ def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
     for i, (e0, e1) in enumerate(evs):
-        torch.cuda._sleep(100000)  # GPU time while the host enqueues the launch
+        torch.cuda._sleep(400000)  # ~0.2 ms of GPU time while the host enqueues the launch
         e0.record(stream)
         bda.bda_attn_fwd(pb, *sets[i % n_rot], o, lse, ws, stream)
         e1.record(stream)
@@ -307,14 +307,15 @@ def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
     with torch.cuda.graph(graph, stream=cap):
         bda.bda_attn_fwd(pb, q, k, v, o, lse, ws, cap)
     for _ in range(10):
-        graph.replay()
+        graph.replay()  # replays launch on the current stream, `stream`
     torch.cuda.synchronize()
     rounds = 200
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record(cap)
+    torch.cuda._sleep(4000000)  # ~2 ms of GPU time: the host enqueues every replay meanwhile
+    g0.record(stream)
     for _ in range(rounds):
         graph.replay()
-    g1.record(cap)
+    g1.record(stream)
     torch.cuda.synchronize()
     st = bda.bda_attn_check_status(ws, stream)
     if st != bda.BDA_OK:
