@@ -319,7 +319,7 @@ def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
     torch.cuda.synchronize()
     st = bda.bda_attn_check_status(ws, stream)
     if st != bda.BDA_OK:
-        raise SystemExit(f"device status {st} after the decode measurement")
+        raise RuntimeError(f"device status {st} after the decode measurement")
     achieved = nbytes / (us * 1e-6) / 1e9
     return {"workload": "decode step: 32 queries over 2,080 keys (2,048 + one block of 32), "
                         "Hq=32, Hkv=8, d=128, forward only",
@@ -531,7 +531,11 @@ def main():
     if e2e is not None:
         out["e2e"] = e2e
     if not args.no_decode:
-        out["decode"] = decode_measurement(bda, dev, stream, hbm)
+        try:
+            out["decode"] = decode_measurement(bda, dev, stream, hbm)
+        except Exception as e:  # a side measurement: the main line is printed regardless
+            torch.cuda.synchronize()
+            out["decode"] = {"error": f"{type(e).__name__}: {e}"}
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, inp)
     print(json.dumps(out), flush=True)
