@@ -265,3 +265,32 @@ def test_bwd_subsets_and_sum_rules():
         np.testing.assert_allclose(dK[:, g].sum(axis=0), 0.0, atol=1e-12)
         want = dO[:, g * G:(g + 1) * G].sum(dim=(0, 1)).numpy()
         np.testing.assert_allclose(dV[:, g].sum(axis=0), want, atol=1e-12)
+
+
+def test_rows_are_convex_combinations_and_lse_normalises():
+    """Each O row lies inside the box spanned by the V rows it may see, and
+    sum_j over the allowed keys of exp(scale q.k - LSE) is 1 (the softmax
+    normaliser), for all three mask kinds."""
+    Hq, Hkv, d, scale = 4, 2, 8, 0.6
+    layouts = [("bc", 4, 0, None, 18), ("sc", 3, 6, None, 15), ("multi", 2, 6, ([2, 1], [2, 6]), 12)]
+    for name, B, P, groups, L in layouts:
+        Q, K, V = rand((L, Hq, d), 90), rand((L, Hkv, d), 91), rand((L, Hkv, d), 92)
+        if name == "bc":
+            O, LSE = oracle.fwd_seq(BC, B, 0, Q, K, V, Hq, Hkv, scale)
+            M = brute.mask_block_causal(L, L, B)
+        elif name == "sc":
+            O, LSE = oracle.fwd_seq(SC, B, P, Q, K, V, Hq, Hkv, scale)
+            M = brute.mask_staircase(L, B, P)
+        else:
+            O, LSE = oracle.fwd_seq_multi(B, P, groups[0], groups[1], Q, K, V, Hq, Hkv, scale)
+            M = brute.mask_staircase_multi(L, B, P, groups[0], groups[1])
+        Qn, Kn, Vn = Q.numpy(), K.numpy(), V.numpy()
+        G = Hq // Hkv
+        for h in range(Hq):
+            for i in range(L):
+                vis = np.nonzero(M[i])[0]
+                Vv = Vn[vis, h // G, :]
+                assert (O[i, h] >= Vv.min(axis=0) - 1e-12).all()
+                assert (O[i, h] <= Vv.max(axis=0) + 1e-12).all()
+                s = scale * Kn[vis, h // G, :] @ Qn[i, h, :]
+                assert abs(np.exp(s - LSE[h, i]).sum() - 1.0) < 1e-12
