@@ -35,7 +35,8 @@ EXPORTED = (
     "bda_attn_fwd",
     "bda_attn_bwd", "bda_attn_bwd_preprocess", "bda_attn_bwd_dkdv", "bda_attn_bwd_dq_convert",
     "bda_attn_count_pairs", "bda_attn_check_status", "bda_status_string",
-    "bda_last_cuda_error", "bda_attn_fwd_noalloc",
+    "bda_last_cuda_error", "bda_attn_fwd_noalloc", "bda_attn_fwd_noalloc_check_status",
+    "bda_testing_arm_wait_timeout",
 )
 
 
@@ -91,6 +92,8 @@ def lib():
             "bda_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "bda_last_cuda_error": ([], ctypes.c_char_p),
             "bda_attn_fwd_noalloc": ([P, M, vp, vp, vp, vp, vp, st], ctypes.c_int),
+            "bda_attn_fwd_noalloc_check_status": ([st], ctypes.c_int),
+            "bda_testing_arm_wait_timeout": ([ctypes.c_int, ctypes.c_ulonglong], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -169,7 +172,7 @@ class Problem:
     @classmethod
     def from_workload(cls, w):
         return cls(w.cu_seqlens_q, w.cu_seqlens_k, w.hq, w.hkv, w.head_dim, w.kind, w.block_size,
-                   w.prefix, w.scale or 0.0)
+                   w.prefix, w.scale or 0.0, getattr(w, "groups", None))
 
     def refs(self):
         return ctypes.byref(self.prob), ctypes.byref(self.mask)
@@ -207,9 +210,21 @@ def bda_attn_fwd(pb: Problem, q, k, v, o, lse, ws, stream=None):
 def bda_attn_fwd_noalloc(pb: Problem, q, k, v, o, lse, stream=None):
     """Forward without a workspace (for callers that cannot allocate device
     memory where they run attention): the plan lives in a fixed 1 MiB array
-    inside the library, shared by every call; overlapping calls race."""
+    inside the library, shared by every call; overlapping calls race, and a
+    stream under graph capture is refused."""
     _check(lib().bda_attn_fwd_noalloc(*pb.refs(), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                       _stream(stream)), "bda_attn_fwd_noalloc")
+
+
+def bda_attn_fwd_noalloc_check_status(stream=None) -> int:
+    """Status of the latest no-alloc forward on the current device (syncs the stream)."""
+    return int(lib().bda_attn_fwd_noalloc_check_status(_stream(stream)))
+
+
+def bda_testing_arm_wait_timeout(stage: int, timeout_ns: int) -> int:
+    """Testing only: the next launch of `stage` (1 forward, 2 dK/dV) lets one
+    bounded wait run out after timeout_ns; 0 disarms."""
+    return int(lib().bda_testing_arm_wait_timeout(int(stage), int(timeout_ns)))
 
 
 def bda_attn_bwd(pb: Problem, q, k, v, o, lse, dout, dq, dk, dv, ws, stream=None):

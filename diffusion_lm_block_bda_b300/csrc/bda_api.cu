@@ -4,6 +4,7 @@
 // argument error), encode the TMA tensor maps over the caller's THD tensors,
 // and launch the kernels on the caller's stream.  No device memory is
 // allocated here; scratch lives in the caller's workspace.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -37,36 +38,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a THD bf16 tensor [rows][heads][d]; box = 64 head-dim elements
-// (128 bytes, 128B swizzle) x box_h heads x box_rows rows.
-bool make_thd_map(CUtensorMap* m, const void* ptr, int d, int heads, int64_t rows, int box_h,
-                  int box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
-  cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(d) * 2 * cuuint64_t(heads)};
-  cuuint32_t box[3] = {64, cuuint32_t(box_h), cuuint32_t(box_rows)};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 3-D map over the fp32 dQ accumulator [rows][heads][d]; box = 32 floats
-// (128 bytes, 128B swizzle) x box_h heads x box_rows rows.
-bool make_f32_map(CUtensorMap* m, const void* ptr, int d, int heads, int64_t rows, int box_h,
-                  int box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
-  cuuint64_t strides[2] = {cuuint64_t(d) * 4, cuuint64_t(d) * 4 * cuuint64_t(heads)};
-  cuuint32_t box[3] = {32, cuuint32_t(box_h), cuuint32_t(box_rows)};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bda_status check_ws(const Shape& s, const void* ws, size_t ws_bytes, bool with_bwd) {
@@ -93,6 +64,99 @@ const uint8_t* plan_ptr(const void* ws) { return static_cast<const uint8_t*>(ws)
 }  // namespace
 
 void note_cuda_error(const char* text) { g_last_cuda_error = text; }
+
+// 3-D map over a THD bf16 tensor [rows][heads][d]; box = 64 head-dim elements
+// (128 bytes, 128B swizzle) x box_h heads x box_rows rows.
+bool make_thd_map(void* map, const void* ptr, int d, int heads, int64_t rows, int box_h,
+                  int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  CUtensorMap* m = static_cast<CUtensorMap*>(map);
+  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
+  cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(d) * 2 * cuuint64_t(heads)};
+  cuuint32_t box[3] = {64, cuuint32_t(box_h), cuuint32_t(box_rows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over the fp32 dQ accumulator [rows][heads][d]; box = 32 floats
+// (128 bytes, 128B swizzle) x box_h heads x box_rows rows.
+bool make_f32_map(void* map, const void* ptr, int d, int heads, int64_t rows, int box_h,
+                  int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  CUtensorMap* m = static_cast<CUtensorMap*>(map);
+  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
+  cuuint64_t strides[2] = {cuuint64_t(d) * 4, cuuint64_t(d) * 4 * cuuint64_t(heads)};
+  cuuint32_t box[3] = {32, cuuint32_t(box_h), cuuint32_t(box_rows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One-shot failure-detection fault (testing only): stage 1 = forward,
+// 2 = backward dK/dV; consumed by the next launch of that stage.
+std::atomic<int> g_fault_stage{0};
+std::atomic<uint64_t> g_fault_timeout_ns{0};
+
+uint64_t take_fault(int stage) {
+  int want = stage;
+  if (!g_fault_stage.compare_exchange_strong(want, 0)) return 0;
+  return g_fault_timeout_ns.load();
+}
+
+FwdArgs make_fwd_args(const Shape& s, const uint8_t* plan, bool with_bwd, void* o, float* lse,
+                      uint32_t* status) {
+  FwdArgs a{};
+  a.items = reinterpret_cast<const FwdItem*>(plan + kHeaderBytes);
+  a.cgroups = s.n_cgroups > 0 ? reinterpret_cast<const int2*>(plan + plan_group_offset(s, with_bwd))
+                              : nullptr;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = status;
+  a.timeout_ns = kTimeoutNs;
+  a.n_groups = s.hq / s.hg;
+  a.hg = s.hg;
+  a.lg_hg = s.lg_hg;
+  a.G = s.G;
+  a.hq = s.hq;
+  a.total_q = int(s.total_q);
+  a.block = s.B;
+  a.scale_log2 = s.scale * 1.4426950408889634f;
+  a.fault_timeout_ns = take_fault(1);
+  a.fault = a.fault_timeout_ns != 0;
+  return a;
+}
+
+BwdArgs make_bwd_args(const Shape& s, const uint8_t* plan, const float* lse, const float* D,
+                      void* dk, void* dv, uint32_t* status) {
+  BwdArgs a{};
+  a.items = reinterpret_cast<const BwdItem*>(plan + kHeaderBytes + sizeof(FwdItem) * size_t(s.n_fwd));
+  a.cgroups = s.n_cgroups > 0 ? reinterpret_cast<const int2*>(plan + plan_group_offset(s, true))
+                              : nullptr;
+  a.lse = lse;
+  a.D = D;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.status = status;
+  a.timeout_ns = kTimeoutNs;
+  a.hq = s.hq;
+  a.hkv = s.hkv;
+  a.G = s.G;
+  a.hg = s.hg;
+  a.lg_hg = s.lg_hg;
+  a.tok = s.tok;
+  a.total_q = int(s.total_q);
+  a.block = s.B;
+  a.scale = s.scale;
+  a.scale_log2 = s.scale * 1.4426950408889634f;
+  a.fault_timeout_ns = take_fault(2);
+  a.fault = a.fault_timeout_ns != 0;
+  return a;
+}
 
 }  // namespace bda
 
@@ -159,20 +223,8 @@ bda_status bda_attn_fwd(const bda_problem* prob, const bda_mask_desc* mask, cons
       !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN) ||
       !make_thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok))
     return tensor_map_error();
-  FwdArgs a{};
-  a.items = reinterpret_cast<const FwdItem*>(plan_ptr(ws) + kHeaderBytes);
-  a.o = static_cast<__nv_bfloat16*>(o);
-  a.lse = lse;
-  a.status = reinterpret_cast<uint32_t*>(ws);
-  a.timeout_ns = kTimeoutNs;
-  a.n_groups = s.hq / s.hg;
-  a.hg = s.hg;
-  a.lg_hg = s.lg_hg;
-  a.G = s.G;
-  a.hq = s.hq;
-  a.total_q = int(s.total_q);
-  a.block = s.B;
-  a.scale_log2 = s.scale * 1.4426950408889634f;
+  const FwdArgs a = make_fwd_args(s, plan_ptr(ws), /*with_bwd=*/true, o, lse,
+                                  reinterpret_cast<uint32_t*>(ws));
   return cuda_status(launch_fwd(s.d, tq, tk, tv, to, a, s.n_fwd, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -221,24 +273,8 @@ bda_status bda_attn_bwd_dkdv(const bda_problem* prob, const bda_mask_desc* mask,
       !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN) ||
       !make_f32_map(&tdq, accsrc, s.d, s.total_q > 0 ? s.hq : 1, rq, hg_map, s.tok))
     return tensor_map_error();
-  BwdArgs a{};
-  a.items = reinterpret_cast<const BwdItem*>(w + kHeaderBytes + sizeof(FwdItem) * size_t(s.n_fwd));
-  a.lse = lse;
-  a.D = reinterpret_cast<const float*>(w + ws_offset_D(s));
-  a.dk = static_cast<__nv_bfloat16*>(dk);
-  a.dv = static_cast<__nv_bfloat16*>(dv);
-  a.status = reinterpret_cast<uint32_t*>(ws);
-  a.timeout_ns = kTimeoutNs;
-  a.hq = s.hq;
-  a.hkv = s.hkv;
-  a.G = s.G;
-  a.hg = s.hg;
-  a.lg_hg = s.lg_hg;
-  a.tok = s.tok;
-  a.total_q = int(s.total_q);
-  a.block = s.B;
-  a.scale = s.scale;
-  a.scale_log2 = s.scale * 1.4426950408889634f;
+  const BwdArgs a = make_bwd_args(s, w, lse, reinterpret_cast<const float*>(w + ws_offset_D(s)),
+                                  dk, dv, reinterpret_cast<uint32_t*>(ws));
   return cuda_status(launch_bwd_dkdv(s.d, tq, tk, tv, tdo, tdq, a, s.n_bwd,
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -291,6 +327,18 @@ bda_status bda_attn_check_status(void* ws, size_t ws_bytes, bda_stream_t stream)
   if ((r = cuda_status(cudaMemsetAsync(ws, 0, sizeof(uint32_t), st))) != BDA_OK) return r;
   if ((r = cuda_status(cudaStreamSynchronize(st))) != BDA_OK) return r;
   return (v & kDeviceTimeoutCode) ? BDA_ERR_DEVICE_TIMEOUT : BDA_ERR_UNSUPPORTED;
+}
+
+bda_status bda_testing_arm_wait_timeout(int stage, unsigned long long timeout_ns) {
+  if (stage == 0) {
+    g_fault_stage.store(0);
+    return BDA_OK;
+  }
+  if ((stage != 1 && stage != 2) || timeout_ns < 1000ull || timeout_ns > 1000000000ull)
+    return BDA_ERR_INVALID_ARG;
+  g_fault_timeout_ns.store(timeout_ns);
+  g_fault_stage.store(stage);
+  return BDA_OK;
 }
 
 const char* bda_last_cuda_error(void) { return g_last_cuda_error; }

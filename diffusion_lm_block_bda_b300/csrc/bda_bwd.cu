@@ -220,13 +220,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const WaitCtx wc{abort_flag, a.status, a.timeout_ns};
+  // Failure-detection testing: CTA 0 leaves its first Q tile un-issued and
+  // unannounced and waits only fault_timeout_ns for it (a.fault is 0 in
+  // normal use).
+  const bool fault_cta = a.fault != 0 && blockIdx.x == 0;
+  const WaitCtx wc{abort_flag, a.status, fault_cta ? a.fault_timeout_ns : a.timeout_ns};
   // Query tile i: token tile t0 (local) and head sub-group.  Tiles are walked
   // from the end of the sequence down, so the CTAs of one sequence, which
   // start together, sweep the same query rows at the same time (L2 reuse of
   // Q, dO and the dQ accumulator).
-  const int n_tok_tiles = (it.q_end - it.q_begin + a.tok - 1) / a.tok;
-  auto tile_t0 = [&](int i) -> int { return it.q_begin + (n_tok_tiles - 1 - i / n_sub) * a.tok; };
+  // The query tokens come in one or two ranges (the second for copy groups
+  // that see the tile's clean keys past groups that do not).
+  const int n_tok_tiles = it.n_tiles1 + (it.q2_end - it.q2_begin + a.tok - 1) / a.tok;
+  auto tile_t0 = [&](int i) -> int {
+    const int m = n_tok_tiles - 1 - i / n_sub;
+    return m < it.n_tiles1 ? it.q_begin + m * a.tok : it.q2_begin + (m - it.n_tiles1) * a.tok;
+  };
   auto tile_h0 = [&](int i) -> int { return kvh * a.G + (i % n_sub) * a.hg; };
 
   bool ok = true;
@@ -272,7 +281,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         const int t0 = tile_t0(i), h0 = tile_h0(i);
-        if (lane == 0) {
+        const bool skip = fault_cta && i == 0;
+        if (lane == 0 && !skip) {
           expect_tx(bar(L::B_QFULL + st), L::TILE);
           for (int c = 0; c < L::CH; ++c)
             tma_load_3d(base + L::Q + st * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + st),
@@ -285,8 +295,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           s_lse[lane + 32 * k] = lv[k];
           s_D[lane + 32 * k] = dv[k];
         }
-        mbar_arrive(bar(L::B_QFULL + st));
-        if (st == 0) ++nq0; else ++nq1;
+        if (!skip) {
+          mbar_arrive(bar(L::B_QFULL + st));
+          if (st == 0) ++nq0; else ++nq1;
+        }
         if (i + 1 < n_iter) fetch(i + 1);
         // dO has one buffer: tile i's once dV of tile i-1 has read it
         if (i >= 1 && !mbar_wait_warp(wc, bar(L::B_DVDONE), uint32_t(i - 1) & 1u)) {
@@ -423,8 +435,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------- softmax
     const int kr = tid;  // TMEM lane == key row of the tile
     const bool key_valid = kr < it.k_len;
-    const KeyRows kq = key_rows(it.kpos0 + kr, it.prefix, a.block, it.lk);
+    // Query positions that see this key: [lo, hi) and [lo2, hi2).
+    const KeyRows kq = key_rows(it.kpos0 + kr, it.prefix, a.block, it.lk, a.cgroups + it.grp_off,
+                                it.n_grp);
     const int q_hi = min(kq.hi - delta, it.lq);  // local query tokens [kq.lo - delta, q_hi)
+    const int q2_lo = kq.lo2 - delta, q2_hi = min(kq.hi2 - delta, it.lq);
     const uint32_t lane_addr = tbase + (uint32_t(warp * 32) << 16);
     const float sl2 = a.scale_log2;
     uint8_t* dsb = gbase + L::DS;
@@ -440,7 +455,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // * hg + head).  Warps whose rows all see the whole tile skip masking.
       const int c_lo = max(lo_c, 0) << a.lg_hg;
       const int c_hi = hi_c <= lo_c ? c_lo : min(hi_c, a.tok) << a.lg_hg;
-      const bool warp_full = __all_sync(0xffffffffu, c_lo == 0 && c_hi >= kTileM);
+      const int lo2_c = key_valid ? q2_lo - t0 : 0;
+      const int hi2_c = key_valid ? q2_hi - t0 : 0;
+      const int c_lo2 = max(lo2_c, 0) << a.lg_hg;
+      const int c_hi2 = hi2_c <= lo2_c ? c_lo2 : min(hi2_c, a.tok) << a.lg_hg;
+      const bool warp_full = __all_sync(0xffffffffu, (c_lo == 0 && c_hi >= kTileM) ||
+                                                         (c_lo2 == 0 && c_hi2 >= kTileM));
       // QFULL publishes the producer's LSE / D staging to these threads.
       if (!mbar_wait2_warp(wc, bar(L::B_QFULL + st), uint32_t(i >> 1) & 1u, bar(L::B_SFULL), ph)) {
         ok = false;
@@ -470,9 +490,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = 32 * c + 2 * j;
-            const uint32_t lo = (col >= c_lo && col < c_hi) ? 0x0000ffffu : 0u;
-            const uint32_t hi = (col + 1 >= c_lo && col + 1 < c_hi) ? 0xffff0000u : 0u;
-            pk[j] &= lo | hi;
+            const bool v0 = (col >= c_lo && col < c_hi) || (col >= c_lo2 && col < c_hi2);
+            const bool v1 = (col + 1 >= c_lo && col + 1 < c_hi) || (col + 1 >= c_lo2 && col + 1 < c_hi2);
+            pk[j] &= (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
           }
         }
 #pragma unroll

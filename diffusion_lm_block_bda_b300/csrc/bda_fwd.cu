@@ -149,7 +149,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const WaitCtx wc{abort_flag, a.status, a.timeout_ns};
+  // Failure-detection testing: CTA 0 leaves its first Q load un-issued and
+  // waits only fault_timeout_ns for it (a.fault is 0 in normal use).
+  const bool fault_cta = a.fault != 0 && blockIdx.x == 0;
+  const WaitCtx wc{abort_flag, a.status, fault_cta ? a.fault_timeout_ns : a.timeout_ns};
 
   // Unit u: work item, head group, and its key tiles.
   struct Unit {
@@ -204,11 +207,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(L::B_QFULL + qb), L::TILE);
-          for (int c = 0; c < L::CH; ++c)
-            tma_load_3d(base + L::Q + qb * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + qb),
-                        c * 64, x.head0, x.it.q_row);
-          ++nq[qb];
+          if (!(fault_cta && k == 0)) {
+            mbar_arrive_expect_tx(bar(L::B_QFULL + qb), L::TILE);
+            for (int c = 0; c < L::CH; ++c)
+              tma_load_3d(base + L::Q + qb * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + qb),
+                          c * 64, x.head0, x.it.q_row);
+            ++nq[qb];
+          }
         }
         for (int n = 0; n < x.n_tiles; ++n, ++g) {
           const int s = g % NST;
@@ -335,7 +340,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const FwdItem& it = x.it;
       const bool row_valid = t_local < it.q_len;
       const int p = it.pos0 + (row_valid ? t_local : it.q_len - 1);
-      const RowKeys rk = row_keys(p, it.prefix, a.block, it.lk);
+      // Copy rows of a multi-block staircase see their group's clean keys.
+      const RowKeys rk = row_keys_g(p, it.prefix, a.block, it.lk, a.cgroups + it.grp_off, it.n_grp);
       float m_ref = -INFINITY;  // running max of scale*log2(e)*S, the reference of P
       float l = 0.f;            // running sum of P (relative to m_ref)
       for (int n = 0; n < x.n_tiles; ++n, ++g) {

@@ -19,25 +19,43 @@ struct Shape {
   int64_t total_q = 0, total_k = 0;
   int n_fwd = 0;    // forward work items (query tiles)
   int n_bwd = 0;    // backward work items (key tiles)
+  int n_cgroups = 0;  // non-empty copy groups (multi-block staircase)
 };
 
 // Validates the problem and mask; fills `s`.  Host-only, launches nothing.
-// A valid multi-block staircase gives BDA_ERR_UNSUPPORTED (no kernel takes it
-// yet) unless count_only, for which it is BDA_OK.
+// A multi-block staircase whose non-empty groups are not in block order
+// (visible decreasing along the sequence) is defined -- count_only accepts
+// it -- but no kernel takes it: BDA_ERR_UNSUPPORTED.
 bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s,
                     bool count_only = false);
 
-size_t plan_bytes(const Shape& s);
+// Plan bytes: header, forward items, (with_bwd) backward items, then the
+// copy-group table (int2 per non-empty group, padded to 16 bytes).
+size_t plan_bytes(const Shape& s, bool with_bwd = true);
+size_t plan_group_offset(const Shape& s, bool with_bwd);
 size_t workspace_bytes(const Shape& s, bool with_bwd);
 size_t ws_offset_D(const Shape& s);      // fp32 [hq][total_q]
 size_t ws_offset_dqacc(const Shape& s);  // fp32 [total_q][hq][d]
 
-// Writes the header and the LPT-ordered work items into `out` (plan_bytes).
-void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, uint8_t* out);
+// Writes the header and the LPT-ordered work items into `out`
+// (plan_bytes(s, with_bwd) bytes; without the backward items, the header
+// records n_bwd = 0).
+void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, uint8_t* out,
+                bool with_bwd = true);
 
 long long count_pairs(const bda_problem* p, const bda_mask_desc* m, const Shape& s);
 
 // Records the text bda_last_cuda_error() returns on this thread.
 void note_cuda_error(const char* text);
+
+// TMA tensor maps over the caller's THD tensors (defined in bda_api.cu).
+// bf16 [rows][heads][d]: box = 64 head-dim elements (128 bytes, 128B
+// swizzle) x box_h heads x box_rows rows.
+bool make_thd_map(void* map, const void* ptr, int d, int heads, int64_t rows, int box_h,
+                  int box_rows);
+// fp32 [rows][heads][d]: box = 32 floats (128 bytes, 128B swizzle) x box_h
+// heads x box_rows rows.
+bool make_f32_map(void* map, const void* ptr, int d, int heads, int64_t rows, int box_h,
+                  int box_rows);
 
 }  // namespace bda

@@ -7,12 +7,22 @@
 // Figure 3 caption).  Block-causal is the staircase with prefix P = Lk (no
 // copies), so one form serves both.  For a query at key position p:
 //   p <  P : keys [0, min(P, (p/B + 1) * B))                 (block-causal)
-//   p >= P : keys [0, P) and its own copy [P + cB, P + cB + B), c = (p-P)/B
-// and, transposed, key j is seen by query positions
-//   j <  P : [ (j/B) * B, Lk )
+//   p >= P : keys [0, V) and its own copy [P + cB, P + cB + B), c = (p-P)/B
+// where V = P for the staircase; and, transposed, key j is seen by query
+// positions
+//   j <  P : [ (j/B) * B, P ) and the copy rows whose V exceeds j
 //   j >= P : [ P + cB, P + cB + B ),  c = (j-P)/B
+// Multi-block staircase (several active blocks per trajectory, the
+// "irregular trajectories" of the announcement thread, Insight 3): the copy
+// rows [P, Lk) are cut into groups, one per active block, and the copies of
+// group g see V = visible_g clean keys.  Groups come in block order, so
+// visible_g does not decrease along the sequence and the copy rows that see
+// a clean key j form one suffix [start of the first group with V > j, Lk).
+// The plan carries the non-empty groups of each sequence as a table of
+// (start position, V) pairs.
 #pragma once
 #include <cstdint>
+#include <vector_types.h>  // int2
 
 #if defined(__CUDACC__)
 #define BDA_HD __host__ __device__ __forceinline__
@@ -43,7 +53,9 @@ struct FwdItem {
   int32_t r2_end;
   int32_t work;      // number of key tiles
   int32_t seq;
-  int32_t pad[4];
+  int32_t grp_off;   // the sequence's copy groups in the plan's table ...
+  int32_t n_grp;     // ... (0: every copy sees the whole prefix)
+  int32_t pad[2];
 };
 static_assert(sizeof(FwdItem) == 64, "FwdItem layout");
 
@@ -57,11 +69,15 @@ struct BwdItem {
   int32_t lq;
   int32_t lk;
   int32_t prefix;    // staircase prefix length; lk for block-causal
-  int32_t q_begin;   // local query tokens [q_begin, q_end) see some key of the tile
-  int32_t q_end;
+  int32_t q_begin;   // local query tokens [q_begin, q_end) and [q2_begin, q2_end)
+  int32_t q_end;     // hold every query that sees some key of the tile; the
+  int32_t q2_begin;  // second range is empty unless copy groups that do not
+  int32_t q2_end;    // see the tile's clean keys sit between the two
+  int32_t n_tiles1;  // query-token tiles of the first range
   int32_t work;      // query tiles to visit per KV head
   int32_t seq;
-  int32_t pad[5];
+  int32_t grp_off;   // as in FwdItem
+  int32_t n_grp;
 };
 static_assert(sizeof(BwdItem) == 64, "BwdItem layout");
 
@@ -74,6 +90,7 @@ struct PlanHeader {
   int32_t tok;
   int32_t total_q;
   int32_t total_k;
+  int32_t n_cgroups;  // entries of the copy-group table (after the items)
 };
 
 // Keys visible to the query at position p: [0, a) U [b, e).
@@ -97,15 +114,56 @@ BDA_HD RowKeys row_keys(int p, int P, int B, int Lk) {
   return r;
 }
 
-// Query positions that see key j: [lo, hi).
+// Copy groups of a multi-block staircase sequence: grp[0..n) = (start, V),
+// starts increasing, V non-decreasing.
+// V of the copy row at position p >= grp[0].x: the last group starting at or
+// before p.
+BDA_HD int group_visible(int p, const int2* grp, int n) {
+  int lo = 0, hi = n - 1;  // invariant: grp[lo].x <= p
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (grp[mid].x <= p) lo = mid; else hi = mid - 1;
+  }
+  return grp[lo].y;
+}
+// First copy row that sees clean key j: the start of the first group with
+// V > j, or Lk if none.
+BDA_HD int group_rows_from(int j, const int2* grp, int n, int Lk) {
+  int lo = 0, hi = n;  // first index with V > j
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (grp[mid].y > j) hi = mid; else lo = mid + 1;
+  }
+  return lo < n ? grp[lo].x : Lk;
+}
+
+// Keys visible to the query at position p when copies see V = grp-table
+// values (n > 0) instead of the whole prefix.
+BDA_HD RowKeys row_keys_g(int p, int P, int B, int Lk, const int2* grp, int n) {
+  RowKeys r = row_keys(p, P, B, Lk);
+  if (n > 0 && p >= P) r.a = group_visible(p, grp, n);
+  return r;
+}
+
+// Query positions that see key j: [lo, hi) and [lo2, hi2) (the second
+// interval is empty unless copy groups that do not see j separate the two).
 struct KeyRows {
-  int lo, hi;
+  int lo, hi, lo2, hi2;
 };
-BDA_HD KeyRows key_rows(int j, int P, int B, int Lk) {
+BDA_HD KeyRows key_rows(int j, int P, int B, int Lk, const int2* grp = nullptr, int n = 0) {
   KeyRows r;
+  r.lo2 = r.hi2 = 0;
   if (j < P) {
     r.lo = (j / B) * B;
     r.hi = Lk;
+    if (n > 0) {
+      const int from = group_rows_from(j, grp, n, Lk);
+      if (from > P) {  // prefix rows, then the copies of the groups that see j
+        r.hi = P;
+        r.lo2 = from;
+        r.hi2 = Lk;
+      }
+    }
   } else {
     r.lo = P + ((j - P) / B) * B;
     const int hi = r.lo + B;

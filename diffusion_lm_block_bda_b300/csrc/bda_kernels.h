@@ -6,12 +6,16 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "bda_host.h"
 #include "bda_internal.h"
 
 namespace bda {
 
 struct FwdArgs {
   const FwdItem* items;
+  // Multi-block staircase: table of copy groups (x = first position of the
+  // group in its sequence, y = clean keys its copies see); null otherwise.
+  const int2* cgroups;
   __nv_bfloat16* o;
   float* lse;
   uint32_t* status;
@@ -24,6 +28,11 @@ struct FwdArgs {
   int total_q;
   int block;
   float scale_log2;  // softmax_scale * log2(e)
+  // Failure-detection testing only (0 in normal use): when set, CTA 0 leaves
+  // its first Q load un-issued, so the wait for it runs out after
+  // fault_timeout_ns and the CTA takes its abort path.
+  int fault;
+  uint64_t fault_timeout_ns;
 };
 
 struct BwdArgs {
@@ -40,7 +49,18 @@ struct BwdArgs {
   int block;
   float scale;       // softmax_scale
   float scale_log2;  // softmax_scale * log2(e)
+  const int2* cgroups;  // as in FwdArgs
+  int fault;           // as in FwdArgs (testing only)
+  uint64_t fault_timeout_ns;
 };
+
+// Kernel arguments for a plan at `plan` (a workspace, or the no-alloc
+// array) holding the items of `s` (with or without the backward items).
+// Consumes a failure-detection test fault armed for that stage, if any.
+FwdArgs make_fwd_args(const Shape& s, const uint8_t* plan, bool with_bwd, void* o, float* lse,
+                      uint32_t* status);
+BwdArgs make_bwd_args(const Shape& s, const uint8_t* plan, const float* lse, const float* D,
+                      void* dk, void* dv, uint32_t* status);
 
 // to: map over O laid out like Q (box 64 x hg x tok, 128-byte swizzle); whole
 // query tiles are written through it.

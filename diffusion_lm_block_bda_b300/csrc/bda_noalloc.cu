@@ -13,11 +13,13 @@
 // (1 MiB): every GPU that loads the library holds it until the process
 // exits.  Host code cannot use the array's name as a device address, so the
 // first call on each device looks the address up with cudaGetSymbolAddress
-// (with that device current) and caches it; make that first call before any
-// stream capture begins on that device.  All calls share the one array and
-// every call overwrites it (plan and a zeroed status word) before its kernel
-// runs: calls whose work overlaps on the GPU -- on different streams, or from
-// different host threads -- race on it and must be serialised by the caller.
+// (with that device current) and caches it.  Each call writes the forward
+// plan (with a zeroed status word) into the array through the parameters of
+// a small copy kernel -- no host-to-device memcpy, so the call never waits
+// for the stream's earlier work -- and then launches the forward.  All calls
+// share the one array: calls whose work overlaps on the GPU (other streams,
+// other host threads) race on it and must be serialised by the caller.  A
+// stream that is being captured into a CUDA graph is refused.
 #include <cstring>
 #include <mutex>
 
@@ -25,51 +27,35 @@
 #include "bda_host.h"
 #include "bda_internal.h"
 #include "bda_kernels.h"
+#include "bda_ptx.cuh"
 
 namespace bda {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 constexpr int kMaxDevices = 64;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Pageable staging copy of the plan: cudaMemcpyAsync returns once it has
-// taken the bytes, so the buffer is free again when the call returns.
+// Host staging of the plan; its bytes travel as kernel parameters, which the
+// launch copies, so the buffer is free again as soon as a launch returns.
 static uint8_t g_plan_staging[kNoAllocScratchBytes];
 static std::mutex g_mu;
 static void* g_scratch_dev[kMaxDevices];
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// One launch carries up to kChunk16 16-byte units (the parameter space holds
+// at most 32,764 bytes).
+constexpr uint32_t kChunk16 = 1984;
+struct PlanChunk {
+  uint32_t offset16;  // destination offset in 16-byte units
+  uint32_t n16;       // units in this chunk
+  uint4 data[kChunk16];
+};
+static_assert(sizeof(PlanChunk) <= 32764, "kernel parameter space");
 
-EncodeTiledFn encoder() {
-  static EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return static_cast<EncodeTiledFn>(nullptr);
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
-bool thd_map(CUtensorMap* m, const void* ptr, int d, int heads, int64_t rows, int box_h,
-             int box_rows) {
-  EncodeTiledFn enc = encoder();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
-  cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(d) * 2 * cuuint64_t(heads)};
-  cuuint32_t box[3] = {64, cuuint32_t(box_h), cuuint32_t(box_rows)};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+__global__ void __launch_bounds__(256) bda_plan_upload_kernel(const __grid_constant__ PlanChunk c) {
+  uint4* dst = reinterpret_cast<uint4*>(g_noalloc_scratch) + c.offset16;
+  for (uint32_t i = threadIdx.x; i < c.n16; i += blockDim.x) dst[i] = c.data[i];
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -79,7 +65,8 @@ bda_status fail_cuda(cudaError_t e) {
   return BDA_ERR_CUDA;
 }
 
-// Device address of g_noalloc_scratch on the current device (looked up once).
+// Device address of g_noalloc_scratch on the current device (looked up once
+// per device, with that device current).
 bda_status scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -95,6 +82,16 @@ bda_status scratch_address(void** out) {
   return BDA_OK;
 }
 
+// Refuses streams under capture: a captured call would bake this call's
+// plan into the graph while the array it writes is shared with every other
+// call.
+bda_status refuse_capture(cudaStream_t cs) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(cs, &cap);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return cap == cudaStreamCaptureStatusNone ? BDA_OK : BDA_ERR_UNSUPPORTED;
+}
+
 }  // namespace
 }  // namespace bda
 
@@ -108,46 +105,62 @@ bda_status bda_attn_fwd_noalloc(const bda_problem* prob, const bda_mask_desc* ma
   Shape s;
   bda_status st = validate(prob, mask, &s);
   if (st != BDA_OK) return st;
-  const size_t need = plan_bytes(s);
+  const size_t need = plan_bytes(s, /*with_bwd=*/false);
   if (need > kNoAllocScratchBytes) return BDA_ERR_WORKSPACE;  // beyond the fixed 1 MiB
   if (s.n_fwd == 0) return BDA_OK;
   if (!q || !k || !v || !o || !lse) return BDA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return BDA_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = refuse_capture(cs)) != BDA_OK) return st;
   CUtensorMap tq, tk, tv, to;
-  if (!thd_map(&tq, q, s.d, s.hq, s.total_q, s.hg, s.tok) ||
-      !thd_map(&tk, k, s.d, s.hkv, s.total_k, 1, kTileN) ||
-      !thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN) ||
-      !thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok)) {
+  if (!make_thd_map(&tq, q, s.d, s.hq, s.total_q, s.hg, s.tok) ||
+      !make_thd_map(&tk, k, s.d, s.hkv, s.total_k, 1, kTileN) ||
+      !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN) ||
+      !make_thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok)) {
     note_cuda_error("cuTensorMapEncodeTiled failed");
     return BDA_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lock(g_mu);
   void* scratch = nullptr;
   if ((st = scratch_address(&scratch)) != BDA_OK) return st;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // The plan (its header carries the zeroed status word) replaces whatever
   // the previous call left in the array.
-  build_plan(prob, mask, s, g_plan_staging);
-  cudaError_t e = cudaMemcpyAsync(scratch, g_plan_staging, need, cudaMemcpyHostToDevice, cs);
-  if (e != cudaSuccess) return fail_cuda(e);
-  FwdArgs a{};
-  a.items = reinterpret_cast<const FwdItem*>(static_cast<uint8_t*>(scratch) + kHeaderBytes);
-  a.o = static_cast<__nv_bfloat16*>(o);
-  a.lse = lse;
-  a.status = static_cast<uint32_t*>(scratch);
-  a.timeout_ns = kTimeoutNs;
-  a.n_groups = s.hq / s.hg;
-  a.hg = s.hg;
-  a.lg_hg = s.lg_hg;
-  a.G = s.G;
-  a.hq = s.hq;
-  a.total_q = int(s.total_q);
-  a.block = s.B;
-  a.scale_log2 = s.scale * 1.4426950408889634f;
-  e = launch_fwd(s.d, tq, tk, tv, to, a, s.n_fwd, cs);
+  build_plan(prob, mask, s, g_plan_staging, /*with_bwd=*/false);
+  const size_t n16 = (need + 15) / 16;
+  static PlanChunk chunk;  // guarded by g_mu; too large for the stack of some threads
+  for (size_t u = 0; u < n16; u += kChunk16) {
+    chunk.offset16 = uint32_t(u);
+    chunk.n16 = uint32_t(n16 - u < kChunk16 ? n16 - u : kChunk16);
+    std::memcpy(chunk.data, g_plan_staging + 16 * u, 16 * size_t(chunk.n16));
+    bda_plan_upload_kernel<<<1, 256, 0, cs>>>(chunk);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  FwdArgs a = make_fwd_args(s, static_cast<const uint8_t*>(scratch), /*with_bwd=*/false, o, lse,
+                            static_cast<uint32_t*>(scratch));
+  cudaError_t e = launch_fwd(s.d, tq, tk, tv, to, a, s.n_fwd, cs);
   if (e != cudaSuccess) return fail_cuda(e);
   return BDA_OK;
+}
+
+bda_status bda_attn_fwd_noalloc_check_status(bda_stream_t stream) {
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  bda_status st = refuse_capture(cs);
+  if (st != BDA_OK) return st;
+  std::lock_guard<std::mutex> lock(g_mu);
+  void* scratch = nullptr;
+  if ((st = scratch_address(&scratch)) != BDA_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return fail_cuda(e);
+  uint32_t v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_noalloc_scratch, sizeof(v), 0, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (v == 0) return BDA_OK;
+  const uint32_t zero = 0;
+  e = cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return (v & kDeviceTimeoutCode) ? BDA_ERR_DEVICE_TIMEOUT : BDA_ERR_UNSUPPORTED;
 }
 
 }  // extern "C"

@@ -33,7 +33,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 int seq_prefix(const bda_mask_desc* m, int s, int lk) {
-  return m->kind == BDA_MASK_STAIRCASE ? m->prefix_len_host[s] : lk;
+  return m->kind != BDA_MASK_BLOCK_CAUSAL ? m->prefix_len_host[s] : lk;
 }
 
 }  // namespace
@@ -73,7 +73,8 @@ bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s, bool
     const int32_t* cq = p->cu_seqlens_q_host;
     const int32_t* ck = p->cu_seqlens_k_host;
     if (cq[0] != 0 || ck[0] != 0) return BDA_ERR_INVALID_ARG;
-    int64_t nf = 0, nb = 0;
+    int64_t nf = 0, nb = 0, ng = 0;
+    bool block_order = true;
     for (int i = 0; i < p->nseq; ++i) {
       const int64_t lq = int64_t(cq[i + 1]) - cq[i];
       const int64_t lk = int64_t(ck[i + 1]) - ck[i];
@@ -90,11 +91,16 @@ bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s, bool
         const int64_t P = m->prefix_len_host[i];
         const int32_t g0 = m->group_offsets_host[i], g1 = m->group_offsets_host[i + 1];
         if (lq != lk || P < 0 || P > lk || g1 < g0) return BDA_ERR_INVALID_ARG;
-        int64_t tokens = 0;
+        int64_t tokens = 0, last_v = -1;
         for (int32_t g = g0; g < g1; ++g) {
           const int64_t c = m->group_copies_host[g], v = m->group_visible_host[g];
           if (c < 0 || v < 0 || v > P) return BDA_ERR_INVALID_ARG;
           tokens += c * m->block_size;
+          if (c > 0) {
+            if (v < last_v) block_order = false;
+            last_v = v;
+            ++ng;
+          }
         }
         if (tokens != lk - P) return BDA_ERR_INVALID_ARG;
       }
@@ -107,16 +113,25 @@ bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s, bool
     if (r.total_q >= (int64_t(1) << 31) || r.total_k >= (int64_t(1) << 31))
       return BDA_ERR_INVALID_ARG;
     if (nf >= (int64_t(1) << 30) / r.hq || nb >= (int64_t(1) << 30)) return BDA_ERR_INVALID_ARG;
+    if (ng >= (int64_t(1) << 30)) return BDA_ERR_INVALID_ARG;
     r.n_fwd = int(nf);
     r.n_bwd = int(nb);
+    r.n_cgroups = int(ng);
+    *s = r;
+    // Groups out of block order are counted but not computed.
+    return block_order || count_only ? BDA_OK : BDA_ERR_UNSUPPORTED;
   }
   *s = r;
-  // The multi-block staircase is validated and counted; no kernel takes it yet.
-  return multi && !count_only ? BDA_ERR_UNSUPPORTED : BDA_OK;
+  return BDA_OK;
 }
 
-size_t plan_bytes(const Shape& s) {
-  return kHeaderBytes + sizeof(FwdItem) * size_t(s.n_fwd) + sizeof(BwdItem) * size_t(s.n_bwd);
+size_t plan_group_offset(const Shape& s, bool with_bwd) {
+  return kHeaderBytes + sizeof(FwdItem) * size_t(s.n_fwd) +
+         (with_bwd ? sizeof(BwdItem) * size_t(s.n_bwd) : 0);
+}
+
+size_t plan_bytes(const Shape& s, bool with_bwd) {
+  return plan_group_offset(s, with_bwd) + ((sizeof(int2) * size_t(s.n_cgroups) + 15) & ~size_t(15));
 }
 
 size_t ws_offset_D(const Shape& s) { return align256(plan_bytes(s)); }
@@ -131,27 +146,46 @@ size_t workspace_bytes(const Shape& s, bool with_bwd) {
          align256(sizeof(float) * size_t(s.total_q) * size_t(s.hq) * size_t(s.d));
 }
 
-void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, uint8_t* out) {
-  std::memset(out, 0, plan_bytes(s));
+void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, uint8_t* out,
+                bool with_bwd) {
+  std::memset(out, 0, plan_bytes(s, with_bwd));
   PlanHeader* h = reinterpret_cast<PlanHeader*>(out);
   h->status = 0;
   h->magic = kPlanMagic;
   h->n_fwd = s.n_fwd;
-  h->n_bwd = s.n_bwd;
+  h->n_bwd = with_bwd ? s.n_bwd : 0;
   h->hg = s.hg;
   h->tok = s.tok;
   h->total_q = int32_t(s.total_q);
   h->total_k = int32_t(s.total_k);
+  h->n_cgroups = s.n_cgroups;
   std::vector<FwdItem> fw;
   std::vector<BwdItem> bw;
   fw.reserve(s.n_fwd);
-  bw.reserve(s.n_bwd);
+  if (with_bwd) bw.reserve(s.n_bwd);
+  // Copy-group table of the multi-block staircase: the non-empty groups of
+  // every sequence, each as (first position, clean keys its copies see).
+  int2* table = reinterpret_cast<int2*>(out + plan_group_offset(s, with_bwd));
+  int n_table = 0;
+  const bool multi = s.kind == BDA_MASK_STAIRCASE_MULTI;
   const int B = s.B;
   for (int sq = 0; sq < s.nseq; ++sq) {
     const int q0 = p->cu_seqlens_q_host[sq], lq = p->cu_seqlens_q_host[sq + 1] - q0;
     const int k0 = p->cu_seqlens_k_host[sq], lk = p->cu_seqlens_k_host[sq + 1] - k0;
     const int P = seq_prefix(m, sq, lk);
     const int delta = lk - lq;
+    const int grp_off = n_table;
+    if (multi) {
+      int start = P;
+      for (int g = m->group_offsets_host[sq]; g < m->group_offsets_host[sq + 1]; ++g) {
+        const int c = m->group_copies_host[g];
+        if (c == 0) continue;
+        table[n_table++] = int2{start, m->group_visible_host[g]};
+        start += c * B;
+      }
+    }
+    const int n_grp = n_table - grp_off;
+    const int2* grp = table + grp_off;
     // forward: query tiles of tok tokens
     for (int t0 = 0; t0 < lq; t0 += s.tok) {
       FwdItem it{};
@@ -162,14 +196,31 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
       it.lk = lk;
       it.prefix = P;
       it.seq = sq;
+      it.grp_off = grp_off;
+      it.n_grp = n_grp;
       const int p_lo = it.pos0, p_hi = it.pos0 + it.q_len - 1;
-      // [0, a(p)) grows with p: tiles inside [0, a(p_lo)) are FULL for every row.
-      const RowKeys lo = row_keys(p_lo, P, B, lk), hi = row_keys(p_hi, P, B, lk);
-      it.n_full = lo.a / kTileN;
-      it.r1_end = ceil_div(hi.a, kTileN);
+      // Rows see [0, a(p)) and their own copy.  Without copy groups a(p)
+      // grows with p; with them, take the extremes over the tile's rows.
+      int a_min, a_max;
+      if (n_grp == 0) {
+        a_min = row_keys(p_lo, P, B, lk).a;
+        a_max = row_keys(p_hi, P, B, lk).a;
+      } else {
+        a_min = lk;
+        a_max = 0;
+        for (int q = p_lo; q <= p_hi; ++q) {
+          const int a = row_keys_g(q, P, B, lk, grp, n_grp).a;
+          a_min = std::min(a_min, a);
+          a_max = std::max(a_max, a);
+        }
+      }
+      // Key tiles inside [0, a_min) are FULL for every row.
+      it.n_full = a_min / kTileN;
+      it.r1_end = ceil_div(a_max, kTileN);
       it.r2_begin = it.r2_end = 0;
       if (p_hi >= P) {  // copy rows: their own copies span [b(first copy row), e(p_hi))
         const RowKeys c = row_keys(std::max(p_lo, P), P, B, lk);
+        const RowKeys hi = row_keys(p_hi, P, B, lk);
         int b0 = c.b / kTileN, b1 = ceil_div(hi.e, kTileN);
         if (b0 <= it.r1_end) {
           it.r1_end = std::max(it.r1_end, b1);
@@ -182,7 +233,7 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
       fw.push_back(it);
     }
     // backward: key tiles of 128 keys
-    for (int kp = 0; kp < lk; kp += kTileN) {
+    for (int kp = 0; with_bwd && kp < lk; kp += kTileN) {
       BwdItem it{};
       it.k_row = k0 + kp;
       it.k_len = std::min(kTileN, lk - kp);
@@ -192,12 +243,37 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
       it.lk = lk;
       it.prefix = P;
       it.seq = sq;
-      const KeyRows first = key_rows(kp, P, B, lk), last = key_rows(kp + it.k_len - 1, P, B, lk);
-      const int hi = std::max(first.hi, last.hi);
-      it.q_begin = std::max(0, first.lo - delta);
-      it.q_end = std::min(lq, hi - delta);
-      if (it.q_end < it.q_begin) it.q_end = it.q_begin;
-      it.work = ceil_div(it.q_end - it.q_begin, s.tok) * (s.G / s.hg);
+      it.grp_off = grp_off;
+      it.n_grp = n_grp;
+      // Query positions that see some key of the tile.  Its first key sees
+      // the most rows of the prefix and of the copy groups; its copy keys
+      // (if any) are seen by their own copies, which follow the prefix.
+      const int kl = kp + it.k_len - 1;
+      const KeyRows first = key_rows(kp, P, B, lk, grp, n_grp);
+      const KeyRows last = key_rows(kl, P, B, lk, grp, n_grp);
+      int lo1 = first.lo, hi1 = std::max(first.hi, kl >= P ? last.hi : 0);
+      int lo2 = first.lo2, hi2 = first.hi2;
+      bool two = hi2 > lo2;
+      if (two && lo2 <= hi1) {  // the ranges touch: one range
+        hi1 = std::max(hi1, hi2);
+        two = false;
+      }
+      if (!two) lo2 = hi2 = 0;
+      auto clip = [&](int x) { return std::min(lq, std::max(0, x - delta)); };
+      it.q_begin = clip(lo1);
+      it.q_end = std::max(it.q_begin, clip(hi1));
+      it.q2_begin = clip(lo2);
+      it.q2_end = std::max(it.q2_begin, clip(hi2));
+      it.n_tiles1 = ceil_div(it.q_end - it.q_begin, s.tok);
+      // The first range's last tile must not reach into the second range
+      // (a query row visited twice would be counted twice): merge them.
+      if (it.q2_end > it.q2_begin && it.q2_begin < it.q_begin + it.n_tiles1 * s.tok) {
+        it.q_end = it.q2_end;
+        it.q2_begin = it.q2_end = 0;
+        it.n_tiles1 = ceil_div(it.q_end - it.q_begin, s.tok);
+      }
+      const int n_tiles2 = ceil_div(it.q2_end - it.q2_begin, s.tok);
+      it.work = (it.n_tiles1 + n_tiles2) * (s.G / s.hg);
       bw.push_back(it);
     }
   }

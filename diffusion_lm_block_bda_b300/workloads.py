@@ -15,18 +15,19 @@ order (1) packed lengths (only for the random-length workload), (2) Q, (3) K,
 tensors go to the GPU and to the oracle.
 """
 from dataclasses import dataclass, field
-from typing import List, Optional
+from typing import List, Optional, Tuple
 
 import torch
 
 BLOCK_CAUSAL = 0
 STAIRCASE = 1
+STAIRCASE_MULTI = 2
 
 
 @dataclass
 class Workload:
     name: str
-    kind: int                      # BLOCK_CAUSAL or STAIRCASE
+    kind: int                      # BLOCK_CAUSAL, STAIRCASE or STAIRCASE_MULTI
     block_size: int
     hq: int
     hkv: int
@@ -38,6 +39,9 @@ class Workload:
     with_bwd: bool = True
     note: str = ""
     extra: dict = field(default_factory=dict)
+    # STAIRCASE_MULTI: per sequence, its copy groups in block order as
+    # (copies, visible clean keys) pairs.
+    groups: Optional[List[List[Tuple[int, int]]]] = None
 
     @property
     def softmax_scale(self) -> float:
@@ -154,8 +158,20 @@ def make_inputs(w: Workload, seed: int = 0, with_dout: Optional[bool] = None):
 
 
 def custom(kind, block_size, hq, hkv, head_dim, seqlens_q, seqlens_k=None, prefix=None,
-           scale=None, name="custom") -> Workload:
+           scale=None, name="custom", groups=None) -> Workload:
     """A workload of arbitrary shape (tests use these for ragged / edge cases)."""
     seqlens_k = list(seqlens_q) if seqlens_k is None else list(seqlens_k)
     return Workload(name, kind, block_size, hq, hkv, head_dim, list(seqlens_q), seqlens_k,
-                    prefix=None if prefix is None else list(prefix), scale=scale)
+                    prefix=None if prefix is None else list(prefix), scale=scale,
+                    groups=None if groups is None else [list(g) for g in groups])
+
+
+def multi_staircase(prefix, groups, block_size=32, hq=32, hkv=8, head_dim=128,
+                    name="staircase_multi") -> Workload:
+    """Multi-block staircase trajectories: sequence s is a clean prefix of
+    prefix[s] tokens followed by its copy groups groups[s] = [(copies,
+    visible), ...] in block order; its length is prefix + sum(copies) * B."""
+    lens = [int(p) + block_size * sum(int(c) for c, _ in g) for p, g in zip(prefix, groups)]
+    return Workload(name, STAIRCASE_MULTI, block_size, hq, hkv, head_dim, lens, list(lens),
+                    prefix=[int(p) for p in prefix],
+                    groups=[[(int(c), int(v)) for c, v in g] for g in groups])

@@ -80,8 +80,10 @@ typedef enum {
    * group_copies[g] copies of B tokens, and each of its copies sees the
    * clean keys [0, group_visible[g]) (the prompt and the clean blocks before
    * its block) and itself only.  STAIRCASE is one group with visible = P.
-   * Validated and counted (bda_attn_count_pairs); the compute calls return
-   * BDA_ERR_UNSUPPORTED for it in this version. */
+   * The compute calls take the groups in block order: along a sequence, the
+   * visible counts of its non-empty groups must not decrease (a layout out
+   * of that order is counted by bda_attn_count_pairs but the other calls
+   * return BDA_ERR_UNSUPPORTED for it). */
   BDA_MASK_STAIRCASE_MULTI = 2
 } bda_mask_kind;
 
@@ -188,20 +190,45 @@ bda_status bda_attn_check_status(void *ws, size_t ws_bytes, bda_stream_t stream)
  * synchronisation an allocation can cause.  Same arguments and results as
  * bda_attn_fwd, minus the workspace: the tile plan and the status word live
  * in a 1 MiB array compiled into the library (every GPU that loads the
- * library holds it until the process exits), and the plan is built and
- * copied on every call.  Allocates nothing (no cudaMalloc/cudaFree).
- *   - BDA_ERR_WORKSPACE if the plan needs more than the 1 MiB array (about
- *     16 thousand 128-row tiles); use bda_attn_fwd with a workspace then.
+ * library holds it until the process exits).  Each call builds the forward
+ * plan on the host and writes it into the array through the parameters of a
+ * small copy kernel on `stream` (no host-to-device memcpy: the call does not
+ * wait for the stream's earlier work), then launches the forward.  Allocates
+ * nothing (no cudaMalloc/cudaFree, no library allocator).
+ *   - BDA_ERR_WORKSPACE if the forward plan needs more than the 1 MiB array
+ *     (about 16 thousand query tiles of 128 rows); use bda_attn_fwd with a
+ *     workspace then.
  *   - The first call on a device looks the array's device address up
- *     (cudaGetSymbolAddress, with that device current); make it before any
- *     stream capture begins on that device.
+ *     (cudaGetSymbolAddress, with that device current).
+ *   - BDA_ERR_UNSUPPORTED if `stream` is being captured into a CUDA graph:
+ *     a captured call would replay this call's plan over an array that
+ *     later calls overwrite.
  *   - Every call overwrites the shared array; calls whose GPU work overlaps
  *     (other streams, other host threads) race on it and must be serialised
- *     by the caller.  A device timeout is recorded in the array's status
- *     word and is not readable through bda_attn_check_status. */
+ *     by the caller. */
 bda_status bda_attn_fwd_noalloc(const bda_problem *prob, const bda_mask_desc *mask, const void *q,
                                 const void *k, const void *v, void *o, float *lse,
                                 bda_stream_t stream);
+
+/* Status of the most recent bda_attn_fwd_noalloc on the current device
+ * (no counterpart on the pages; the same role as bda_attn_check_status for
+ * the no-alloc array): synchronises `stream`, reads the array's status word,
+ * clears it, and returns BDA_ERR_DEVICE_TIMEOUT or BDA_ERR_UNSUPPORTED as
+ * bda_attn_check_status does.  Call it after the forward whose status is
+ * wanted and before the next no-alloc call (which resets the word).
+ * Allocates nothing; refuses a stream under capture. */
+bda_status bda_attn_fwd_noalloc_check_status(bda_stream_t stream);
+
+/* Failure-detection testing hook (no counterpart on the pages).  Arms a
+ * one-shot fault for the next launch of `stage` in this process (1 = the
+ * forward kernel, of bda_attn_fwd or bda_attn_fwd_noalloc; 2 = the backward
+ * dK/dV kernel): CTA 0 of that launch leaves its first Q load un-issued,
+ * waits timeout_ns (1 us .. 1 s) for it, records BDA_ERR_DEVICE_TIMEOUT in
+ * the status word, lets its in-flight copies and MMAs land, frees its TMEM
+ * and returns.  Nothing faults and no wait is unbounded; the outputs of that
+ * launch are unspecified.  stage 0 disarms.  BDA_ERR_INVALID_ARG otherwise.
+ * Never armed unless called. */
+bda_status bda_testing_arm_wait_timeout(int stage, unsigned long long timeout_ns);
 
 const char *bda_status_string(bda_status s);
 

@@ -26,6 +26,7 @@ from . import build as _build
 
 BLOCK_CAUSAL = 0
 STAIRCASE = 1
+STAIRCASE_MULTI = 2
 
 _lib = None
 
@@ -148,9 +149,10 @@ def bwd_seq(kind, B, P, Q, K, V, dO, hq, hkv, scale, kv_heads=None, qrows=None, 
     return dQ, dK, dV
 
 
-def fwd(kind, B, cu_q, cu_k, prefix, Q, K, V, hq, hkv, scale, heads=None):
-    """Packed varlen forward: cu_q/cu_k int [nseq+1]; prefix [nseq] (staircase)
-    or None.  Returns (O [T_q][Hq][d], LSE [Hq][T_q]) fp64."""
+def fwd(kind, B, cu_q, cu_k, prefix, Q, K, V, hq, hkv, scale, heads=None, groups=None):
+    """Packed varlen forward: cu_q/cu_k int [nseq+1]; prefix [nseq] (staircase
+    kinds) or None; groups (STAIRCASE_MULTI) per sequence a list of (copies,
+    visible) pairs.  Returns (O [T_q][Hq][d], LSE [Hq][T_q]) fp64."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     cu_q = [int(x) for x in cu_q]
     cu_k = [int(x) for x in cu_k]
@@ -161,15 +163,21 @@ def fwd(kind, B, cu_q, cu_k, prefix, Q, K, V, hq, hkv, scale, heads=None):
         q0, q1, k0, k1 = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
         if q1 == q0:
             continue
-        P = _prefix(kind, prefix, s, k1 - k0)
-        o, l = fwd_seq(kind, B, P, Q[q0:q1], K[k0:k1], V[k0:k1], hq, hkv, scale, heads)
+        if kind == STAIRCASE_MULTI:
+            g = groups[s]
+            o, l = fwd_seq_multi(B, int(prefix[s]), [c for c, _ in g], [v for _, v in g],
+                                 Q[q0:q1], K[k0:k1], V[k0:k1], hq, hkv, scale, heads)
+        else:
+            P = _prefix(kind, prefix, s, k1 - k0)
+            o, l = fwd_seq(kind, B, P, Q[q0:q1], K[k0:k1], V[k0:k1], hq, hkv, scale, heads)
         O[q0:q1] = o
         LSE[:, q0:q1] = l
     return O, LSE
 
 
-def bwd(kind, B, cu_q, cu_k, prefix, Q, K, V, dO, hq, hkv, scale, kv_heads=None):
-    """Packed varlen backward.  Returns (dQ, dK, dV) fp64 in THD layout."""
+def bwd(kind, B, cu_q, cu_k, prefix, Q, K, V, dO, hq, hkv, scale, kv_heads=None, groups=None):
+    """Packed varlen backward (arguments as for fwd).  Returns (dQ, dK, dV)
+    fp64 in THD layout."""
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
     cu_q = [int(x) for x in cu_q]
     cu_k = [int(x) for x in cu_k]
@@ -180,13 +188,19 @@ def bwd(kind, B, cu_q, cu_k, prefix, Q, K, V, dO, hq, hkv, scale, kv_heads=None)
         q0, q1, k0, k1 = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
         if k1 == k0:
             continue
-        P = _prefix(kind, prefix, s, k1 - k0)
         if q1 == q0:
             dK[k0:k1] = 0.0
             dV[k0:k1] = 0.0
             continue
-        dq, dk, dv = bwd_seq(kind, B, P, Q[q0:q1], K[k0:k1], V[k0:k1], dO[q0:q1], hq, hkv,
-                             scale, kv_heads)
+        if kind == STAIRCASE_MULTI:
+            g = groups[s]
+            dq, dk, dv = bwd_seq_multi(B, int(prefix[s]), [c for c, _ in g], [v for _, v in g],
+                                       Q[q0:q1], K[k0:k1], V[k0:k1], dO[q0:q1], hq, hkv, scale,
+                                       kv_heads)
+        else:
+            P = _prefix(kind, prefix, s, k1 - k0)
+            dq, dk, dv = bwd_seq(kind, B, P, Q[q0:q1], K[k0:k1], V[k0:k1], dO[q0:q1], hq, hkv,
+                                 scale, kv_heads)
         dQ[q0:q1] = dq
         dK[k0:k1] = dk
         dV[k0:k1] = dv
@@ -263,10 +277,14 @@ def bwd_seq_multi(B, P, copies, visible, Q, K, V, dO, hq, hkv, scale, kv_heads=N
     return dQ, dK, dV
 
 
-def count_pairs_packed(kind, B, cu_q, cu_k, prefix) -> int:
+def count_pairs_packed(kind, B, cu_q, cu_k, prefix, groups=None) -> int:
     """Allowed (i, j) pairs summed over the packed sequences (per head)."""
     n = 0
     for s in range(len(cu_q) - 1):
         Lq, Lk = int(cu_q[s + 1] - cu_q[s]), int(cu_k[s + 1] - cu_k[s])
-        n += count_pairs(kind, B, _prefix(kind, prefix, s, Lk), Lq, Lk)
+        if kind == STAIRCASE_MULTI:
+            g = groups[s]
+            n += count_pairs_multi(B, int(prefix[s]), [c for c, _ in g], [v for _, v in g], Lq)
+        else:
+            n += count_pairs(kind, B, _prefix(kind, prefix, s, Lk), Lq, Lk)
     return n

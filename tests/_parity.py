@@ -80,7 +80,7 @@ def compare_full(w, inputs, got, with_bwd=True, kv_heads=None):
         heads = (kv_heads[0] * G, kv_heads[1] * G)
     O, LSE = oracle.fwd(w.kind, w.block_size, w.cu_seqlens_q, w.cu_seqlens_k, w.prefix,
                         inputs["q"], inputs["k"], inputs["v"], w.hq, w.hkv, w.softmax_scale,
-                        heads=heads)
+                        heads=heads, groups=w.groups)
     hs = slice(None) if heads is None else slice(*heads)
     ks = slice(None) if kv_heads is None else slice(*kv_heads)
     res = {}
@@ -89,7 +89,7 @@ def compare_full(w, inputs, got, with_bwd=True, kv_heads=None):
     if with_bwd:
         dQ, dK, dV = oracle.bwd(w.kind, w.block_size, w.cu_seqlens_q, w.cu_seqlens_k, w.prefix,
                                 inputs["q"], inputs["k"], inputs["v"], inputs["dout"], w.hq,
-                                w.hkv, w.softmax_scale, kv_heads=kv_heads)
+                                w.hkv, w.softmax_scale, kv_heads=kv_heads, groups=w.groups)
         res["dq"] = check_grad(got["dq"][:, hs].numpy(), dQ[:, hs], "dQ", w.name)
         res["dk"] = check_grad(got["dk"][:, ks].numpy(), dK[:, ks], "dK", w.name)
         res["dv"] = check_grad(got["dv"][:, ks].numpy(), dV[:, ks], "dV", w.name)
@@ -107,20 +107,31 @@ def compare_sampled(w, inputs, got, seqs, kv_heads, qrows_fn, krows_fn, with_bwd
     acc = {n: ([], []) for n in ("o", "lse", "dq", "dk", "dv")}
     for s in seqs:
         q0, q1, k0, k1 = cq[s], cq[s + 1], ck[s], ck[s + 1]
-        P = w.prefix[s] if w.kind == W.STAIRCASE else (k1 - k0)
         qr = qrows_fn(q1 - q0)
         Q, K, V = inputs["q"][q0:q1], inputs["k"][k0:k1], inputs["v"][k0:k1]
-        O, LSE = oracle.fwd_seq(w.kind, w.block_size, P, Q, K, V, w.hq, w.hkv, w.softmax_scale,
-                                heads=(hs.start, hs.stop), rows=qr)
+        if w.kind == W.STAIRCASE_MULTI:
+            g = w.groups[s]
+            lay = (w.block_size, w.prefix[s], [c for c, _ in g], [v for _, v in g])
+            O, LSE = oracle.fwd_seq_multi(*lay, Q, K, V, w.hq, w.hkv, w.softmax_scale,
+                                          heads=(hs.start, hs.stop), rows=qr)
+        else:
+            P = w.prefix[s] if w.kind == W.STAIRCASE else (k1 - k0)
+            O, LSE = oracle.fwd_seq(w.kind, w.block_size, P, Q, K, V, w.hq, w.hkv,
+                                    w.softmax_scale, heads=(hs.start, hs.stop), rows=qr)
         acc["o"][0].append(got["o"][q0:q1][qr][:, hs].numpy())
         acc["o"][1].append(O[:, hs])
         acc["lse"][0].append(got["lse"][hs, q0:q1][:, qr].numpy())
         acc["lse"][1].append(LSE[hs])
         if with_bwd:
             kr = krows_fn(k1 - k0)
-            dQ, dK, dV = oracle.bwd_seq(w.kind, w.block_size, P, Q, K, V, inputs["dout"][q0:q1],
-                                        w.hq, w.hkv, w.softmax_scale, kv_heads=kv_heads,
-                                        qrows=qr, krows=kr)
+            if w.kind == W.STAIRCASE_MULTI:
+                dQ, dK, dV = oracle.bwd_seq_multi(*lay, Q, K, V, inputs["dout"][q0:q1], w.hq,
+                                                  w.hkv, w.softmax_scale, kv_heads=kv_heads,
+                                                  qrows=qr, krows=kr)
+            else:
+                dQ, dK, dV = oracle.bwd_seq(w.kind, w.block_size, P, Q, K, V,
+                                            inputs["dout"][q0:q1], w.hq, w.hkv, w.softmax_scale,
+                                            kv_heads=kv_heads, qrows=qr, krows=kr)
             acc["dq"][0].append(got["dq"][q0:q1][qr][:, hs].numpy())
             acc["dq"][1].append(dQ[:, hs])
             acc["dk"][0].append(got["dk"][k0:k1][kr][:, ks].numpy())

@@ -151,29 +151,50 @@ def test_count_pairs_named_workloads():
         assert bda.bda_attn_count_pairs(Problem.from_workload(W.named(name))) == want
 
 
-# Multi-block staircase: described at the boundary, validated and counted on
-# the host; no kernel takes it yet, so every compute call reports
-# BDA_ERR_UNSUPPORTED before launching anything.
+# Multi-block staircase: validated and counted on the host like the oracle;
+# groups in block order (visible non-decreasing over a sequence's non-empty
+# groups) are planned and computed, other layouts are counted only.
 MULTI = dict(kind=bda.BDA_MASK_STAIRCASE_MULTI, cu_seqlens_q=[0, 224, 576],
              cu_seqlens_k=[0, 224, 576], prefix_len=[128, 64],
              groups=[[(2, 64), (1, 128)], [(4, 32), (0, 0), (5, 64)]])
 
 
-def test_multi_block_staircase_is_counted_like_the_oracle_and_unsupported():
+def _multi_oracle_count(spec):
+    want = 0
+    for s, g in enumerate(spec["groups"]):
+        n = spec["cu_seqlens_q"][s + 1] - spec["cu_seqlens_q"][s]
+        want += oracle.count_pairs_multi(32, spec["prefix_len"][s], [c for c, _ in g],
+                                         [v for _, v in g], n)
+    return want
+
+
+def test_multi_block_staircase_is_counted_like_the_oracle_and_planned():
     pb = _pb(**MULTI)
     L = bda.lib()
-    want = 0
-    for s, g in enumerate(MULTI["groups"]):
-        n = MULTI["cu_seqlens_q"][s + 1] - MULTI["cu_seqlens_q"][s]
-        want += oracle.count_pairs_multi(32, MULTI["prefix_len"][s], [c for c, _ in g],
-                                         [v for _, v in g], n)
-    assert L.bda_attn_count_pairs(*pb.refs()) == want
+    assert L.bda_attn_count_pairs(*pb.refs()) == _multi_oracle_count(MULTI)
+    n = L.bda_attn_plan_size(*pb.refs())
+    assert n > 0 and L.bda_attn_workspace_size(*pb.refs(), 1) > n
+    buf = torch.zeros(n, dtype=torch.uint8)
+    assert L.bda_attn_plan_host(*pb.refs(), buf.data_ptr(), buf.numel()) == bda.BDA_OK
+
+
+def test_multi_block_staircase_out_of_block_order_is_counted_not_computed():
+    spec = {**MULTI, "groups": [[(2, 64), (1, 32)], [(4, 32), (0, 0), (5, 64)]]}
+    pb = _pb(**spec)
+    L = bda.lib()
+    assert L.bda_attn_count_pairs(*pb.refs()) == _multi_oracle_count(spec)
     assert L.bda_attn_plan_size(*pb.refs()) == 0
-    assert L.bda_attn_workspace_size(*pb.refs(), 1) == 0
     buf = torch.zeros(1 << 16, dtype=torch.uint8)
     assert L.bda_attn_plan_host(*pb.refs(), buf.data_ptr(), buf.numel()) == bda.BDA_ERR_UNSUPPORTED
     assert _fwd_status(pb, ws_bytes=1 << 30) == bda.BDA_ERR_UNSUPPORTED
     assert L.bda_attn_bwd(*pb.refs(), *[FAKE] * 9, FAKE, 1 << 30, None) == bda.BDA_ERR_UNSUPPORTED
+
+
+def test_testing_hook_arguments():
+    assert bda.bda_testing_arm_wait_timeout(3, 10**6) == bda.BDA_ERR_INVALID_ARG
+    assert bda.bda_testing_arm_wait_timeout(1, 10) == bda.BDA_ERR_INVALID_ARG
+    assert bda.bda_testing_arm_wait_timeout(1, 10**10) == bda.BDA_ERR_INVALID_ARG
+    assert bda.bda_testing_arm_wait_timeout(0, 0) == bda.BDA_OK
 
 
 @pytest.mark.parametrize("kw", [

@@ -213,8 +213,12 @@ def test_packed_replay_c3():
     seqs = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 5})
     compare_sampled(w, inp, got, seqs=seqs, kv_heads=(0, 1), qrows_fn=_sample_rows,
                     krows_fn=_tail_keys)
+    # every key (and every query row) of the shortest and of the longest
+    # sequence: the longest holds the longest dK/dV query loops of the batch
     compare_sampled(w, inp, got, seqs=[int(np.argmin(lens))], kv_heads=(7, 8),
-                    qrows_fn=_sample_rows, krows_fn=lambda L: list(range(L)))
+                    qrows_fn=lambda L: list(range(L)), krows_fn=lambda L: list(range(L)))
+    compare_sampled(w, inp, got, seqs=[int(np.argmax(lens))], kv_heads=(3, 4),
+                    qrows_fn=lambda L: list(range(L)), krows_fn=lambda L: list(range(L)))
     check_sum_rules(w, inp, got)
 
 
@@ -222,6 +226,11 @@ def test_long_block_causal_c5():
     w = W.named("c5")
     inp = W.make_inputs(w, seed=0)
     got = gpu_run(w, inp)
+    # dK/dV element by element on the first key tile (keys 0..127: every one
+    # of the 32,768 query rows sees them, the dK/dV kernel's longest loop, 1,024
+    # query tiles), on a mid-sequence tile and on the last keys
+    L = w.seqlens_k[0]
+    keys = list(range(128)) + list(range(L // 2, L // 2 + 128)) + _tail_keys(L, 96)
     compare_sampled(w, inp, got, seqs=[0], kv_heads=(0, 1),
-                    qrows_fn=lambda L: _sample_rows(L, 24), krows_fn=lambda L: _tail_keys(L, 96))
+                    qrows_fn=lambda n: _sample_rows(n, 24), krows_fn=lambda n: keys)
     check_sum_rules(w, inp, got)

@@ -3,8 +3,9 @@ decoded and compared exhaustively with the oracle's explicit mask.
 
 Forward: every allowed (query, key) pair of every query tile falls in exactly
 one listed key tile; tiles marked FULL hold only allowed pairs; no listed tile
-is empty.  Backward: the query-token range of each key tile holds every query
-that sees one of its keys.  Order: forward longest unit first, backward
+is empty.  Backward: the query-token tiles of each key tile (one or two
+ranges) hold every query that sees one of its keys, and no query twice.
+Multi-block staircase layouts are checked against the oracle's mask too.  Order: forward longest unit first, backward
 sequence-major (longest sequences first, longest key tiles first inside each);
 a list schedule over 148 SMs ends within one unit of max(total / 148, longest
 unit)."""
@@ -21,9 +22,9 @@ from diffusion_lm_block_bda_b300 import Problem, workloads as W
 HDR = 256
 ITEM_INTS = 16
 FWD_FIELDS = ["q_row", "q_len", "pos0", "k_row", "lk", "prefix", "n_full", "r1_end", "r2_begin",
-              "r2_end", "work", "seq"]
+              "r2_end", "work", "seq", "grp_off", "n_grp"]
 BWD_FIELDS = ["k_row", "k_len", "kpos0", "q_row", "lq", "lk", "prefix", "q_begin", "q_end",
-              "work", "seq"]
+              "q2_begin", "q2_end", "n_tiles1", "work", "seq", "grp_off", "n_grp"]
 
 
 def decode(pb):
@@ -33,9 +34,15 @@ def decode(pb):
     hdr = a[:HDR // 4]
     magic, n_fwd, n_bwd, hg, tok = int(hdr[1]) & 0xffffffff, int(hdr[2]), int(hdr[3]), int(hdr[4]), int(hdr[5])
     assert magic == 0x42444131
-    items = a[HDR // 4:].reshape(-1, ITEM_INTS)
+    n_items = n_fwd + n_bwd
+    items = a[HDR // 4:HDR // 4 + n_items * ITEM_INTS].reshape(-1, ITEM_INTS)
     fw = [dict(zip(FWD_FIELDS, map(int, r))) for r in items[:n_fwd]]
     bw = [dict(zip(BWD_FIELDS, map(int, r))) for r in items[n_fwd:n_fwd + n_bwd]]
+    n_cg = int(hdr[8])
+    table = a[HDR // 4 + n_items * ITEM_INTS:][:2 * n_cg].reshape(-1, 2)
+    assert a.size * 4 == HDR + 64 * n_items + -(-8 * n_cg // 16) * 16
+    for it in fw + bw:
+        it["groups"] = [tuple(map(int, r)) for r in table[it["grp_off"]:it["grp_off"] + it["n_grp"]]]
     return fw, bw, hg, tok
 
 
@@ -52,6 +59,11 @@ def check_plan(w):
     masks = []
     for s in range(w.nseq):
         lq, lk = cq[s + 1] - cq[s], ck[s + 1] - ck[s]
+        if w.kind == W.STAIRCASE_MULTI:
+            g = w.groups[s]
+            masks.append(oracle.mask_multi(w.block_size, w.prefix[s], [c for c, _ in g],
+                                           [v for _, v in g], lq) if lq else None)
+            continue
         P = w.prefix[s] if w.kind == W.STAIRCASE else lk
         masks.append(oracle.mask(w.kind, w.block_size, P, lq, lk) if lq and lk else None)
     # forward coverage
@@ -83,14 +95,22 @@ def check_plan(w):
         assert it["k_row"] == ck[s] + kp and it["k_len"] == min(128, ck[s + 1] - ck[s] - kp)
         M = masks[s]
         if M is None:
-            assert it["q_end"] == it["q_begin"]
+            assert it["q_end"] == it["q_begin"] and it["q2_end"] == it["q2_begin"]
             continue
+        lq = cq[s + 1] - cq[s]
+        n1 = -(-(it["q_end"] - it["q_begin"]) // tok)
+        n2 = -(-(it["q2_end"] - it["q2_begin"]) // tok)
+        assert it["n_tiles1"] == n1
+        # the tiles the kernel walks: no query token twice, every seeing row inside
+        tokens = [t for i in range(n1) for t in range(it["q_begin"] + i * tok,
+                                                        it["q_begin"] + (i + 1) * tok)]
+        tokens += [t for i in range(n2) for t in range(it["q2_begin"] + i * tok,
+                                                         it["q2_begin"] + (i + 1) * tok)]
+        assert len(tokens) == len(set(tokens)), ("query token visited twice", s, kp)
         sees = M[:, kp:kp + it["k_len"]].any(axis=1)
-        idx = np.nonzero(sees)[0]
-        if idx.size:
-            assert it["q_begin"] <= idx.min() and idx.max() < it["q_end"]
-        n_tok = it["q_end"] - it["q_begin"]
-        assert it["work"] == -(-n_tok // tok) * (G // hg)
+        idx = set(np.nonzero(sees)[0].tolist())
+        assert idx <= set(t for t in tokens if t < lq), ("seeing row not visited", s, kp)
+        assert it["work"] == (n1 + n2) * (G // hg)
     assert sorted(it["kpos0"] + ck[it["seq"]] for it in bw) == sorted(
         ck[s] + kp for s in range(w.nseq) for kp in range(0, ck[s + 1] - ck[s], 128))
     # Order: forward longest-first; backward sequence-major (sequences by total
@@ -120,7 +140,26 @@ def check_plan(w):
     return fw, bw
 
 
+def random_multi_workload(rng):
+    """Multi-block staircase layouts with groups in block order (visible
+    non-decreasing), some groups empty."""
+    B = rng.choice([1, 5, 16, 32, 64, 128])
+    hq, hkv = rng.choice([(4, 4), (8, 2), (32, 8), (16, 1)])
+    prefix, groups = [], []
+    for _ in range(rng.randint(1, 3)):
+        P = rng.randint(0, 400)
+        vis = sorted(rng.randint(0, P) for _ in range(rng.randint(0, 4)))
+        g = [(rng.choice([0, 1, 2, 3, 6]), v) for v in vis]
+        if P == 0 and sum(c for c, _ in g) == 0:
+            g = [(1, 0)]
+        prefix.append(P)
+        groups.append(g)
+    return W.multi_staircase(prefix, groups, block_size=B, hq=hq, hkv=hkv)
+
+
 def random_workload(rng):
+    if rng.random() < 0.3:
+        return random_multi_workload(rng)
     kind = rng.choice([W.BLOCK_CAUSAL, W.STAIRCASE])
     B = rng.choice([1, 5, 16, 32, 64, 128, 200])
     hq, hkv = rng.choice([(4, 4), (8, 2), (32, 8), (16, 1), (6, 2)])
@@ -144,8 +183,19 @@ def random_workload(rng):
 
 def test_planner_random_exhaustive():
     rng = random.Random(11)
-    for _ in range(60):
+    for _ in range(90):
         check_plan(random_workload(rng))
+
+
+def test_planner_multi_block_staircase_layouts():
+    # the hand-drawn layouts' shapes, scaled up, and 4 groups x 8 copies after 1024
+    ws = [W.multi_staircase([6 * 32], [[(2, 2 * 32), (1, 6 * 32)]], block_size=32, hq=8, hkv=2),
+          W.multi_staircase([1024] * 2, [[(8, 256), (8, 512), (8, 768), (8, 1024)]] * 2),
+          W.multi_staircase([1000, 130], [[(3, 0), (2, 640), (1, 1000)], [(0, 5), (4, 130)]],
+                            block_size=16, hq=8, hkv=2)]
+    for w in ws:
+        fw, bw = check_plan(w)
+        assert any(it["n_grp"] > 0 for it in fw)
 
 
 @pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4"])
