@@ -56,18 +56,52 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-side", action="store_true",
+                   help="skip the staircase (c4) and long-sequence (c5) measurements")
+    p.add_argument("--stub", action="store_true",
+                   help="launcher check without a GPU: every rank shards the batch and reports "
+                        "(gloo), no kernel runs")
     return p.parse_args()
 
 
 # ------------------------------------------------------------ distributed
+def free_port():
+    import socket
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    return port
+
+
+def launch_ranks(args):
+    """`--gpus N` without an outer launcher: start N ranks (one process per
+    GPU) through torch.distributed.run and return its exit status.  Under a
+    launcher whose world size differs from --gpus, refuse."""
+    world = os.environ.get("WORLD_SIZE")
+    if world is not None:
+        if int(world) != args.gpus:
+            raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}")
+        return None
+    if args.gpus <= 1:
+        return None
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", str(free_port()), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if args.stub:
+            dist.init_process_group("gloo")
+        else:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     return world, rank, local
 
 
@@ -97,16 +131,35 @@ def sum_over_ranks(x, world):
 
 # --------------------------------------------------------------- workload
 def rank_workload(world, rank):
-    """Global batch of 16 * world packed sequences (seed 0), LPT-sharded."""
+    """Global batch of 16 * world packed sequences (seed 0), LPT-sharded:
+    (this rank's workload, its sequence ids, every rank's useful-pair load)."""
     from diffusion_lm_block_bda_b300 import sharding
     gen = torch.Generator().manual_seed(0)
     lens = W.packed_lengths(gen, n=16 * world)
     full = W.Workload("packed_block_causal_16xU512_4096_B32", W.BLOCK_CAUSAL, 32, 32, 8, 128,
                       lens, list(lens))
     if world == 1:
-        return full, list(range(len(lens)))
-    shards = sharding.lpt_shard(sharding.sequence_costs(full), world)
-    return sharding.subset(full, shards[rank], f"_rank{rank}"), shards[rank]
+        return full, list(range(len(lens))), None
+    costs = sharding.sequence_costs(full)
+    shards = sharding.lpt_shard(costs, world)
+    loads = [sum(costs[i] for i in sh) for sh in shards]
+    return sharding.subset(full, shards[rank], f"_rank{rank}"), shards[rank], loads
+
+
+def run_stub(args, world, rank):
+    """The multi-rank launch path without a GPU: every rank derives its shard
+    of the global batch and rank 0 prints what each rank got."""
+    w, seq_ids, loads = rank_workload(world, rank)
+    shards = [seq_ids]
+    if world > 1:
+        import torch.distributed as dist
+        shards = [None] * world
+        dist.all_gather_object(shards, seq_ids)
+        dist.barrier()
+    if rank == 0:
+        print(json.dumps({"stub": True, "n_gpus": world, "gpus_active": world,
+                          "global_sequences": 16 * world, "shards": shards,
+                          "shard_pairs": loads}), flush=True)
 
 
 # ------------------------------------------------------------------ clocks
@@ -167,7 +220,9 @@ def measured_peaks():
     return 1800.0, 1400.0, 6400.0, "fallback"
 
 
-KERNEL_SOURCES = ("diffusion_lm_block_bda_b300/csrc/bda_bwd.cu", "diffusion_lm_block_bda_b300/csrc/bda_ptx.cuh",
+KERNEL_SOURCES = ("diffusion_lm_block_bda_b300/csrc/bda_bwd.cu",
+                  "diffusion_lm_block_bda_b300/csrc/bda_fwd.cu",
+                  "diffusion_lm_block_bda_b300/csrc/bda_ptx.cuh",
                   "diffusion_lm_block_bda_b300/csrc/bda_internal.h",
                   "diffusion_lm_block_bda_b300/csrc/bda_kernels.h")
 
@@ -181,10 +236,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the backward dK/dV kernel from the committed ncu
-    summary; None when absent or taken on a different build of the kernel
-    (the summary records a hash of the kernel's sources)."""
+def profiled_traffic(kernel="bwd_dkdv"):
+    """DRAM bytes per launch of a kernel ("bwd_dkdv" or "fwd") from the
+    committed ncu summary; None when absent or taken on a different build of
+    the kernels (the summary records a hash of the kernels' sources)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -192,7 +247,7 @@ def profiled_traffic():
         j = json.load(f)
     if j.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
-    return j.get("bwd_dkdv_bytes_per_launch")
+    return j.get(f"{kernel}_bytes_per_launch")
 
 
 # -------------------------------------------------------------- reference
@@ -204,14 +259,13 @@ def run_reference(args, world, rank):
         return
     import numpy as np
     import oracle
-    from diffusion_lm_block_bda_b300 import Problem, bda_attn_count_pairs
-    w, _ = rank_workload(1, 0)
+    w, _, _ = rank_workload(1, 0)
     inp = W.make_inputs(w, seed=0)
     s = int(np.argsort(w.seqlens_q)[len(w.seqlens_q) // 2])
     L = w.seqlens_q[s]
     c = w.cu_seqlens_q
     sl = slice(c[s], c[s + 1])
-    pairs = bda_attn_count_pairs(Problem([0, L], [0, L], 32, 8, 128, W.BLOCK_CAUSAL, 32))
+    pairs = oracle.count_pairs(W.BLOCK_CAUSAL, 32, L, L, L)  # useful work, counted by the oracle
     G = w.hq // w.hkv
     flops = 14.0 * w.head_dim * G * pairs
     times = []
@@ -244,13 +298,11 @@ def cpu_baseline(w, inp):
     sequence, all heads, fwd+bwd."""
     import numpy as np
     import oracle
-    from diffusion_lm_block_bda_b300 import Problem, bda_attn_count_pairs
     s = int(np.argsort(w.seqlens_q)[len(w.seqlens_q) // 2])
     L = w.seqlens_q[s]
     c = w.cu_seqlens_q
     sl = slice(c[s], c[s + 1])
-    pairs = bda_attn_count_pairs(Problem([0, L], [0, L], w.hq, w.hkv, w.head_dim, w.kind,
-                                         w.block_size))
+    pairs = oracle.count_pairs(w.kind, w.block_size, L, L, L)
     t0 = time.perf_counter()
     oracle.fwd_seq(w.kind, w.block_size, L, inp["q"][sl], inp["k"][sl], inp["v"][sl], w.hq,
                    w.hkv, w.softmax_scale)
@@ -329,14 +381,81 @@ def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
             "graph_us": g0.elapsed_time(g1) * 1e3 / rounds, "graph_rounds": rounds}
 
 
+# ---------------------------------------------------------- side workloads
+def side_measurement(bda, dev, stream, name, peak_burst, reps):
+    """Useful TFLOPS of one more workload of the pages' kind, fwd + bwd, on
+    inputs resident in HBM: "staircase" = 8 trajectories of a 1,024-token
+    prefix and 16 copies of a 32-token block; "long" = one 32,768-token
+    sequence, block 64.  The plan is built once; each rep is the forward and
+    the three backward stages, back to back, timed with CUDA events on the
+    launching stream (median per stage)."""
+    from diffusion_lm_block_bda_b300 import Problem
+    w = W.named(name)
+    inp = W.make_inputs(w, seed=0)
+    pb = Problem.from_workload(w)
+    pairs = bda.bda_attn_count_pairs(pb)
+    fwd_fl, bwd_fl = 4.0 * w.head_dim * w.hq * pairs, 10.0 * w.head_dim * w.hq * pairs
+    q, k, v, dout = (inp[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((w.hq, pb.total_q), dtype=torch.float32, device=dev)
+    ws = torch.zeros(bda.bda_attn_workspace_size(pb, True), dtype=torch.uint8, device=dev)
+    host = torch.empty(bda.bda_attn_plan_size(pb), dtype=torch.uint8).pin_memory()
+
+    bda.bda_attn_plan(pb, host, ws, stream)  # the same plan serves every rep
+
+    def rep(ev=None):
+        if ev:
+            ev[0].record(stream)
+        bda.bda_attn_fwd(pb, q, k, v, o, lse, ws, stream)
+        if ev:
+            ev[1].record(stream)
+        bda.bda_attn_bwd_preprocess(pb, o, dout, ws, stream)
+        if ev:
+            ev[2].record(stream)
+        bda.bda_attn_bwd_dkdv(pb, q, k, v, lse, dout, dk, dv, ws, stream)
+        if ev:
+            ev[3].record(stream)
+        bda.bda_attn_bwd_dq_convert(pb, dq, ws, stream)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(3):
+        rep()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(reps)]
+    for e in evs:
+        rep(e)
+    torch.cuda.synchronize()
+    if bda.bda_attn_check_status(ws, stream) != bda.BDA_OK:
+        raise RuntimeError(f"device status reports an error in the {name} measurement")
+    med = [statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(4)]
+    fwd_ms, pre_ms, dkdv_ms, conv_ms = med
+    step_ms = sum(med)
+    useful = fwd_fl + bwd_fl
+    return {"workload": w.note or w.name, "useful_pairs_per_head": pairs,
+            "useful_gflop": useful / 1e9, "reps": reps,
+            "stages_ms": {"fwd": round(fwd_ms, 4), "bwd_preprocess": round(pre_ms, 4),
+                          "bwd_dkdv": round(dkdv_ms, 4), "bwd_dq_convert": round(conv_ms, 4)},
+            "ms_per_step": step_ms, "value": useful / (step_ms * 1e-3) / 1e12, "unit": UNIT,
+            "frac_of_peak": useful / (step_ms * 1e-3) / 1e12 / peak_burst,
+            "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12,
+            "bwd_dkdv_tflops": bwd_fl / (dkdv_ms * 1e-3) / 1e12,
+            "peak": peak_burst, "peak_kind": "bf16 burst (measured)"}
+
+
 # ------------------------------------------------------------------ native
 def main():
     args = parse()
+    rc = launch_ranks(args)
+    if rc is not None:
+        raise SystemExit(rc)
     if args.impl == "reference":
         # CPU-only arm: rank 0 runs the oracle, other ranks have nothing to do.
         run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
     world, rank, local = dist_setup(args)
+    if args.stub:
+        run_stub(args, world, rank)
+        return
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")
     import diffusion_lm_block_bda_b300 as bda
@@ -344,7 +463,7 @@ def main():
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w, seq_ids = rank_workload(world, rank)
+    w, seq_ids, shard_pairs = rank_workload(world, rank)
     inp = W.make_inputs(w, seed=rank)
     pb = Problem.from_workload(w)
     pairs = bda.bda_attn_count_pairs(pb)
@@ -495,10 +614,21 @@ def main():
     total_flops = sum_over_ranks(step_flops, world)
     value = total_flops / (ms * 1e-3) / 1e12
     peak_burst, peak_sust, hbm, peak_kind = measured_peaks()
-    dkdv_ms = stage_ms[3]
-    achieved = bwd_flops / (dkdv_ms * 1e-3) / 1e12
     stages = dict(zip(["plan", "fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"],
                       [round(x, 4) for x in stage_ms]))
+    # Both tensor-core kernels against the measured bf16 burst peak: the timed
+    # region is a fraction of a second of back-to-back steps, not a
+    # seconds-long run under the power cap.
+    def roofline(kernel, flops, ms_):
+        achieved = flops / (ms_ * 1e-3) / 1e12
+        return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak_burst,
+                "unit": "TFLOP/s", "frac": achieved / peak_burst,
+                "peak_kind": f"bf16 burst ({peak_kind})", "ms_per_launch": ms_,
+                "algorithmic_flops_per_launch": flops}
+    rl_dkdv = roofline("bda_bwd_dkdv", bwd_flops, stage_ms[3])
+    rl_dkdv["traffic"] = profiled_traffic()
+    rl_fwd = roofline("bda_fwd", fwd_flops, stage_ms[1])
+    rl_fwd["traffic"] = profiled_traffic("fwd")
 
     if rank != 0:
         return
@@ -514,18 +644,16 @@ def main():
                    "l2": "inputs larger than L2 (Q, O, dO, dQ 0.3 GB each)",
                    "parallelism": f"dp{world} (whole sequences, LPT-sharded)" if world > 1 else "1 GPU"},
         "frac_of_peak": value / peak_burst,
+        "timed_region_ms": total_ms,
         "stages_ms": stages,
-        # The dK/dV kernel is timed inside the long back-to-back step loop
-        # (under the power cap), so its denominator is the sustained bf16
-        # peak; its fraction of the burst peak is given beside it.
-        "roofline": {"kernel": "bda_bwd_dkdv", "bound": "tensor", "achieved": achieved,
-                     "peak": peak_sust, "unit": "TFLOP/s", "frac": achieved / peak_sust,
-                     "peak_kind": f"bf16 sustained ({peak_kind})",
-                     "frac_of_burst": achieved / peak_burst,
-                     "traffic": profiled_traffic()},
+        "roofline": rl_dkdv,
+        "rooflines": {"bda_bwd_dkdv": rl_dkdv, "bda_fwd": rl_fwd},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
     }
+    if world > 1:
+        out["gpus_active"] = world
+        out["shard_pairs_per_rank"] = shard_pairs
     out["fwd_tflops"] = fwd_flops / (stage_ms[1] * 1e-3) / 1e12
     out["bwd_tflops"] = bwd_flops / (sum(stage_ms[2:]) * 1e-3) / 1e12
     if e2e is not None:
@@ -536,6 +664,13 @@ def main():
         except Exception as e:  # a side measurement: the main line is printed regardless
             torch.cuda.synchronize()
             out["decode"] = {"error": f"{type(e).__name__}: {e}"}
+    if not args.no_side:
+        for key, name, reps in (("staircase", "c4", 20), ("long", "c5", 5)):
+            try:
+                out[key] = side_measurement(bda, dev, stream, name, peak_burst, reps)
+            except Exception as e:  # a side measurement: the main line is printed regardless
+                torch.cuda.synchronize()
+                out[key] = {"error": f"{type(e).__name__}: {e}"}
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, inp)
     print(json.dumps(out), flush=True)

@@ -74,3 +74,36 @@ def test_lpt_shard_single_rank_and_errors():
     assert sharding.lpt_shard([], 3) == [[], [], []]
     with pytest.raises(ValueError):
         sharding.lpt_shard([1], 0)
+
+
+def test_bench_launches_its_own_ranks_and_shards_the_batch():
+    """`bench.py --gpus 2` without an outer launcher starts two ranks itself
+    (torch.distributed.run; here with gloo and no kernel, --stub): both ranks
+    start, and their shards partition the 32-sequence global batch."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--stub"],
+                         capture_output=True, text=True, timeout=300, env=env, cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = [ln for ln in res.stdout.splitlines() if ln.startswith("{")][-1]
+    out = json.loads(line)
+    assert out["n_gpus"] == 2 and out["gpus_active"] == 2
+    shards = out["shards"]
+    assert len(shards) == 2 and all(shards)
+    assert sorted(i for sh in shards for i in sh) == list(range(32))
+    loads = out["shard_pairs"]
+    assert max(loads) - min(loads) <= max(loads) * 0.25
+
+
+def test_bench_refuses_a_world_size_that_differs_from_gpus():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="3", RANK="0", LOCAL_RANK="0")
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--stub"],
+                         capture_output=True, text=True, timeout=120, env=env, cwd=root)
+    assert res.returncode != 0 and "WORLD_SIZE=3" in res.stderr
