@@ -319,19 +319,23 @@ def cpu_baseline(w, inp):
 def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
     """The decode step (32 new queries over a 2,080-key context: 2,048
     committed tokens + the active block; Hq=32, Hkv=8, d=128; forward only)
-    is bound by HBM bandwidth and latency, not by the tensor cores.  As in a
-    denoising loop, where every layer's KV cache has left L2 by the time the
-    layer comes round again while the kernels' code stays cached, the timed
-    launches rotate through 16 copies of Q, K and V (144 MB, more than L2):
-    each launch reads its copy from HBM.  The stream is held busy while the
-    host enqueues, so the events bracket GPU time only.  `us`: median time of
-    the forward; `achieved` = the minimum bytes (Q, K, V read once, O and LSE
-    written) / `us`.  `graph_us`: one copy's forward captured in a CUDA graph
-    and replayed back to back (everything in L2), GPU time per replay."""
+    is bound by HBM bandwidth and latency, not by the tensor cores.  Its
+    forward runs the split kernel (each query tile's 17 key tiles as 136
+    CTAs) and the combine kernel.  As in a denoising loop, where every
+    layer's KV cache has left L2 by the time the layer comes round again
+    while the kernels' code stays cached, the timed launches rotate through 16
+    copies of Q, K and V (144 MB, more than L2): each launch reads its copy
+    from HBM.  The stream is held busy while the host enqueues, so the events
+    bracket GPU time only.  `us`: median time of the forward; `achieved` =
+    the minimum bytes (Q, K, V read once, O and LSE written) / `us`.
+    `graph_us`: one copy's forward captured in a CUDA graph and replayed back
+    to back (everything in L2), GPU time per replay.  `fp8`: the same step
+    over an e4m3 KV cache (bda_attn_fwd_fp8kv), whose minimum bytes count K
+    and V at one byte per element."""
     from diffusion_lm_block_bda_b300 import Problem
     w = W.named("c2")
     pb = Problem.from_workload(w)
-    sets = []
+    sets, sets8 = [], []
     for i in range(n_rot):
         inp = W.make_inputs(w, seed=i, with_dout=False)
         sets.append(tuple(inp[n].to(dev) for n in ("q", "k", "v")))
@@ -341,18 +345,40 @@ def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
     ws = torch.zeros(bda.bda_attn_workspace_size(pb, False), dtype=torch.uint8, device=dev)
     host = torch.empty(bda.bda_attn_plan_size(pb), dtype=torch.uint8).pin_memory()
     bda.bda_attn_plan(pb, host, ws, stream)
+    k_scale = torch.empty(w.hkv, dtype=torch.float32, device=dev)
+    v_scale = torch.empty(w.hkv, dtype=torch.float32, device=dev)
+    for (qq, kk, vv) in sets:
+        k8 = torch.empty(kk.shape, dtype=torch.uint8, device=dev)
+        v8 = torch.empty(vv.shape, dtype=torch.uint8, device=dev)
+        bda.bda_kv_fp8_scales(kk, k_scale, stream)
+        bda.bda_kv_fp8_scales(vv, v_scale, stream)
+        bda.bda_kv_quantize_fp8(kk, k8, k_scale, stream)
+        bda.bda_kv_quantize_fp8(vv, v8, v_scale, stream)
+        sets8.append((qq, k8, v8))
     nbytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, lse))
-    for x in sets:
-        bda.bda_attn_fwd(pb, *x, o, lse, ws, stream)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(reps)]
-    for i, (e0, e1) in enumerate(evs):
-        torch.cuda._sleep(400000)  # ~0.2 ms of GPU time while the host enqueues the launch
-        e0.record(stream)
-        bda.bda_attn_fwd(pb, *sets[i % n_rot], o, lse, ws, stream)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    us = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+    nbytes8 = nbytes - (k.numel() + v.numel())
+
+    def run(i, fp8):
+        if fp8:
+            bda.bda_attn_fwd_fp8kv(pb, *sets8[i % n_rot], k_scale, v_scale, o, lse, ws, stream)
+        else:
+            bda.bda_attn_fwd(pb, *sets[i % n_rot], o, lse, ws, stream)
+
+    def timed(fp8):
+        for i in range(n_rot):
+            run(i, fp8)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for i, (e0, e1) in enumerate(evs):
+            torch.cuda._sleep(400000)  # ~0.2 ms of GPU time while the host enqueues the launch
+            e0.record(stream)
+            run(i, fp8)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+
+    us = timed(False)
+    us8 = timed(True)
     cap = torch.cuda.Stream(device=dev)
     cap.wait_stream(stream)
     graph = torch.cuda.CUDAGraph()
@@ -373,12 +399,17 @@ def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
     if st != bda.BDA_OK:
         raise RuntimeError(f"device status {st} after the decode measurement")
     achieved = nbytes / (us * 1e-6) / 1e9
+    achieved8 = nbytes8 / (us8 * 1e-6) / 1e9
     return {"workload": "decode step: 32 queries over 2,080 keys (2,048 + one block of 32), "
                         "Hq=32, Hkv=8, d=128, forward only",
+            "kernels": "split forward (17 key tiles x 8 head groups = 136 CTAs) + combine",
             "bound": "hbm", "bytes": nbytes, "us": us, "achieved": achieved,
             "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
             "l2": f"launches rotate through {n_rot} Q/K/V copies (> L2)",
-            "graph_us": g0.elapsed_time(g1) * 1e3 / rounds, "graph_rounds": rounds}
+            "graph_us": g0.elapsed_time(g1) * 1e3 / rounds, "graph_rounds": rounds,
+            "fp8": {"bytes": nbytes8, "us": us8, "achieved": achieved8, "peak": hbm_gbs,
+                    "unit": "GB/s", "frac": achieved8 / hbm_gbs,
+                    "kv": "e4m3 codes, one fp32 scale per KV head"}}
 
 
 # ---------------------------------------------------------- side workloads

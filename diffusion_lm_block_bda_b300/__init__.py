@@ -36,7 +36,8 @@ EXPORTED = (
     "bda_attn_bwd", "bda_attn_bwd_preprocess", "bda_attn_bwd_dkdv", "bda_attn_bwd_dq_convert",
     "bda_attn_count_pairs", "bda_attn_check_status", "bda_status_string",
     "bda_last_cuda_error", "bda_attn_fwd_noalloc", "bda_attn_fwd_noalloc_check_status",
-    "bda_testing_arm_wait_timeout",
+    "bda_testing_arm_wait_timeout", "bda_attn_fwd_fp8kv", "bda_kv_quantize_fp8",
+    "bda_kv_fp8_scales", "bda_testing_force_forward_kernel",
 )
 
 
@@ -94,6 +95,12 @@ def lib():
             "bda_attn_fwd_noalloc": ([P, M, vp, vp, vp, vp, vp, st], ctypes.c_int),
             "bda_attn_fwd_noalloc_check_status": ([st], ctypes.c_int),
             "bda_testing_arm_wait_timeout": ([ctypes.c_int, ctypes.c_ulonglong], ctypes.c_int),
+            "bda_attn_fwd_fp8kv": ([P, M, vp, vp, vp, vp, vp, vp, vp, vp, sz, st], ctypes.c_int),
+            "bda_kv_quantize_fp8": ([vp, vp, vp, ctypes.c_longlong, ctypes.c_int, ctypes.c_int, st],
+                                    ctypes.c_int),
+            "bda_kv_fp8_scales": ([vp, vp, ctypes.c_longlong, ctypes.c_int, ctypes.c_int, st],
+                                  ctypes.c_int),
+            "bda_testing_force_forward_kernel": ([ctypes.c_int], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -225,6 +232,33 @@ def bda_testing_arm_wait_timeout(stage: int, timeout_ns: int) -> int:
     """Testing only: the next launch of `stage` (1 forward, 2 dK/dV) lets one
     bounded wait run out after timeout_ns; 0 disarms."""
     return int(lib().bda_testing_arm_wait_timeout(int(stage), int(timeout_ns)))
+
+
+def bda_attn_fwd_fp8kv(pb: Problem, q, k8, v8, k_scale, v_scale, o, lse, ws, stream=None):
+    """Forward over an FP8 (e4m3) KV cache: k8/v8 uint8 codes [T_k][Hkv][d],
+    k_scale/v_scale fp32 [Hkv] dequantisation scales (device)."""
+    _check(lib().bda_attn_fwd_fp8kv(*pb.refs(), _ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale),
+                                    _ptr(v_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _stream(stream)), "bda_attn_fwd_fp8kv")
+
+
+def bda_kv_quantize_fp8(x, x8, scale, stream=None):
+    """e4m3 codes of x / scale[h] for bf16 x [rows][heads][d] into uint8 x8."""
+    rows, heads, d = x.shape
+    _check(lib().bda_kv_quantize_fp8(_ptr(x), _ptr(x8), _ptr(scale), rows, heads, d,
+                                     _stream(stream)), "bda_kv_quantize_fp8")
+
+
+def bda_kv_fp8_scales(x, scale, stream=None):
+    """Per-head scales max|x| / 448 (1 for an all-zero head) into fp32 scale [heads]."""
+    rows, heads, d = x.shape
+    _check(lib().bda_kv_fp8_scales(_ptr(x), _ptr(scale), rows, heads, d, _stream(stream)),
+           "bda_kv_fp8_scales")
+
+
+def bda_testing_force_forward_kernel(which: int) -> int:
+    """Testing only: 0 the plan's choice, 1 persistent forward, 2 split forward."""
+    return int(lib().bda_testing_force_forward_kernel(int(which)))
 
 
 def bda_attn_bwd(pb: Problem, q, k, v, o, lse, dout, dq, dk, dv, ws, stream=None):

@@ -108,9 +108,19 @@ uint64_t take_fault(int stage) {
   return g_fault_timeout_ns.load();
 }
 
+// Forward kernel choice, testing only: 0 = by the plan (the split kernel
+// when the plan splits its items), 1 = always the persistent kernel, 2 =
+// always the split kernel.
+std::atomic<int> g_force_fwd{0};
+
 FwdArgs make_fwd_args(const Shape& s, const uint8_t* plan, bool with_bwd, void* o, float* lse,
-                      uint32_t* status) {
+                      uint32_t* status, uint8_t* ws_parts) {
   FwdArgs a{};
+  a.dec = reinterpret_cast<const DecItem*>(plan + plan_dec_offset(s, with_bwd));
+  if (ws_parts && s.n_parts > 0) {
+    a.part_o = reinterpret_cast<float*>(ws_parts + ws_offset_parts(s));
+    a.part_lse = reinterpret_cast<float*>(ws_parts + ws_offset_part_lse(s));
+  }
   a.items = reinterpret_cast<const FwdItem*>(plan + kHeaderBytes);
   a.cgroups = s.n_cgroups > 0 ? reinterpret_cast<const int2*>(plan + plan_group_offset(s, with_bwd))
                               : nullptr;
@@ -156,6 +166,21 @@ BwdArgs make_bwd_args(const Shape& s, const uint8_t* plan, const float* lse, con
   a.fault_timeout_ns = take_fault(2);
   a.fault = a.fault_timeout_ns != 0;
   return a;
+}
+
+// 3-D map over e4m3 codes [rows][heads][d] (bytes); box = d codes x 1 head x
+// 128 rows, no swizzle (the split kernel's threads expand the tile).
+bool make_fp8_map(void* map, const void* ptr, int d, int heads, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  CUtensorMap* m = static_cast<CUtensorMap*>(map);
+  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
+  cuuint64_t strides[2] = {cuuint64_t(d), cuuint64_t(d) * cuuint64_t(heads)};
+  cuuint32_t box[3] = {cuuint32_t(d), 1, cuuint32_t(kTileN)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace bda
@@ -224,8 +249,61 @@ bda_status bda_attn_fwd(const bda_problem* prob, const bda_mask_desc* mask, cons
       !make_thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok))
     return tensor_map_error();
   const FwdArgs a = make_fwd_args(s, plan_ptr(ws), /*with_bwd=*/true, o, lse,
-                                  reinterpret_cast<uint32_t*>(ws));
-  return cuda_status(launch_fwd(s.d, tq, tk, tv, to, a, s.n_fwd, reinterpret_cast<cudaStream_t>(stream)));
+                                  reinterpret_cast<uint32_t*>(ws), static_cast<uint8_t*>(ws));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // Problems that fill few SMs (a decode step) take the split kernel; the
+  // persistent kernel ignores the plan's split units and computes every item.
+  const int force = g_force_fwd.load();
+  if (force == 2 || (force == 0 && s.split_c > 0))
+    return cuda_status(launch_decode(s.d, false, tq, tk, tv, a, s.n_dec, s.n_fwd, s.n_parts > 0, cs));
+  return cuda_status(launch_fwd(s.d, tq, tk, tv, to, a, s.n_fwd, cs));
+}
+
+bda_status bda_attn_fwd_fp8kv(const bda_problem* prob, const bda_mask_desc* mask, const void* q,
+                              const void* k8, const void* v8, const float* k_scale,
+                              const float* v_scale, void* o, float* lse, void* ws, size_t ws_bytes,
+                              bda_stream_t stream) {
+  Shape s;
+  bda_status st = validate(prob, mask, &s);
+  if (st != BDA_OK) return st;
+  if ((st = check_ws(s, ws, ws_bytes, false)) != BDA_OK) return st;
+  if (s.n_fwd == 0) return BDA_OK;
+  if (!q || !k8 || !v8 || !k_scale || !v_scale || !o || !lse) return BDA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return BDA_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv;
+  if (!make_thd_map(&tq, q, s.d, s.hq, s.total_q, s.hg, s.tok) ||
+      !make_fp8_map(&tk, k8, s.d, s.hkv, s.total_k) || !make_fp8_map(&tv, v8, s.d, s.hkv, s.total_k))
+    return tensor_map_error();
+  FwdArgs a = make_fwd_args(s, plan_ptr(ws), /*with_bwd=*/true, o, lse,
+                            reinterpret_cast<uint32_t*>(ws), static_cast<uint8_t*>(ws));
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  return cuda_status(launch_decode(s.d, true, tq, tk, tv, a, s.n_dec, s.n_fwd, s.n_parts > 0,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bda_status bda_kv_quantize_fp8(const void* x, void* x8, const float* scale, long long rows,
+                               int heads, int head_dim, bda_stream_t stream) {
+  if (rows < 0 || heads <= 0 || (head_dim != 64 && head_dim != 128)) return BDA_ERR_INVALID_ARG;
+  if (rows == 0) return BDA_OK;
+  if (!x || !x8 || !scale || !aligned16(x) || !aligned16(x8) ||
+      (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return BDA_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_fp8(static_cast<const __nv_bfloat16*>(x),
+                                         static_cast<uint8_t*>(x8), scale, rows, heads, head_dim,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bda_status bda_kv_fp8_scales(const void* x, float* scale, long long rows, int heads, int head_dim,
+                             bda_stream_t stream) {
+  if (rows < 0 || heads <= 0 || heads > 4096 || (head_dim != 64 && head_dim != 128))
+    return BDA_ERR_INVALID_ARG;
+  if (!scale || (reinterpret_cast<uintptr_t>(scale) & 3u) || (rows > 0 && (!x || !aligned16(x))))
+    return BDA_ERR_INVALID_ARG;
+  return cuda_status(launch_fp8_scales(static_cast<const __nv_bfloat16*>(x), scale, rows, heads,
+                                       head_dim, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 bda_status bda_attn_bwd_preprocess(const bda_problem* prob, const bda_mask_desc* mask,
@@ -338,6 +416,12 @@ bda_status bda_testing_arm_wait_timeout(int stage, unsigned long long timeout_ns
     return BDA_ERR_INVALID_ARG;
   g_fault_timeout_ns.store(timeout_ns);
   g_fault_stage.store(stage);
+  return BDA_OK;
+}
+
+bda_status bda_testing_force_forward_kernel(int which) {
+  if (which < 0 || which > 2) return BDA_ERR_INVALID_ARG;
+  g_force_fwd.store(which);
   return BDA_OK;
 }
 

@@ -168,7 +168,10 @@ __device__ __forceinline__ void expect_tx(uint32_t bar, uint32_t bytes) {
 // The dQ partial of each query tile leaves TMEM through shared memory and is
 // added to the fp32 accumulator by TMA reduce-add (per-element atomic), so no
 // thread issues global atomics.
-template <int D>
+// MULTI: the plan has copy groups (multi-block staircase), so a key is seen
+// by up to two query intervals and a key tile by up to two query ranges;
+// block-causal and single-block staircase plans run the one-interval code.
+template <int D, bool MULTI>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -231,9 +234,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // Q, dO and the dQ accumulator).
   // The query tokens come in one or two ranges (the second for copy groups
   // that see the tile's clean keys past groups that do not).
-  const int n_tok_tiles = it.n_tiles1 + (it.q2_end - it.q2_begin + a.tok - 1) / a.tok;
+  const int n_tok_tiles =
+      MULTI ? it.n_tiles1 + (it.q2_end - it.q2_begin + a.tok - 1) / a.tok : it.n_tiles1;
   auto tile_t0 = [&](int i) -> int {
     const int m = n_tok_tiles - 1 - i / n_sub;
+    if (!MULTI) return it.q_begin + m * a.tok;
     return m < it.n_tiles1 ? it.q_begin + m * a.tok : it.q2_begin + (m - it.n_tiles1) * a.tok;
   };
   auto tile_h0 = [&](int i) -> int { return kvh * a.G + (i % n_sub) * a.hg; };
@@ -436,8 +441,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int kr = tid;  // TMEM lane == key row of the tile
     const bool key_valid = kr < it.k_len;
     // Query positions that see this key: [lo, hi) and [lo2, hi2).
-    const KeyRows kq = key_rows(it.kpos0 + kr, it.prefix, a.block, it.lk, a.cgroups + it.grp_off,
-                                it.n_grp);
+    const KeyRows kq = MULTI ? key_rows(it.kpos0 + kr, it.prefix, a.block, it.lk,
+                                        a.cgroups + it.grp_off, it.n_grp)
+                             : key_rows(it.kpos0 + kr, it.prefix, a.block, it.lk);
     const int q_hi = min(kq.hi - delta, it.lq);  // local query tokens [kq.lo - delta, q_hi)
     const int q2_lo = kq.lo2 - delta, q2_hi = min(kq.hi2 - delta, it.lq);
     const uint32_t lane_addr = tbase + (uint32_t(warp * 32) << 16);
@@ -455,12 +461,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // * hg + head).  Warps whose rows all see the whole tile skip masking.
       const int c_lo = max(lo_c, 0) << a.lg_hg;
       const int c_hi = hi_c <= lo_c ? c_lo : min(hi_c, a.tok) << a.lg_hg;
-      const int lo2_c = key_valid ? q2_lo - t0 : 0;
-      const int hi2_c = key_valid ? q2_hi - t0 : 0;
-      const int c_lo2 = max(lo2_c, 0) << a.lg_hg;
-      const int c_hi2 = hi2_c <= lo2_c ? c_lo2 : min(hi2_c, a.tok) << a.lg_hg;
+      int c_lo2 = 0, c_hi2 = 0;
+      if (MULTI) {
+        const int lo2_c = key_valid ? q2_lo - t0 : 0;
+        const int hi2_c = key_valid ? q2_hi - t0 : 0;
+        c_lo2 = max(lo2_c, 0) << a.lg_hg;
+        c_hi2 = hi2_c <= lo2_c ? c_lo2 : min(hi2_c, a.tok) << a.lg_hg;
+      }
       const bool warp_full = __all_sync(0xffffffffu, (c_lo == 0 && c_hi >= kTileM) ||
-                                                         (c_lo2 == 0 && c_hi2 >= kTileM));
+                                                         (MULTI && c_lo2 == 0 && c_hi2 >= kTileM));
       // QFULL publishes the producer's LSE / D staging to these threads.
       if (!mbar_wait2_warp(wc, bar(L::B_QFULL + st), uint32_t(i >> 1) & 1u, bar(L::B_SFULL), ph)) {
         ok = false;
@@ -490,8 +499,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = 32 * c + 2 * j;
-            const bool v0 = (col >= c_lo && col < c_hi) || (col >= c_lo2 && col < c_hi2);
-            const bool v1 = (col + 1 >= c_lo && col + 1 < c_hi) || (col + 1 >= c_lo2 && col + 1 < c_hi2);
+            const bool v0 = (col >= c_lo && col < c_hi) || (MULTI && col >= c_lo2 && col < c_hi2);
+            const bool v1 = (col + 1 >= c_lo && col + 1 < c_hi) ||
+                            (MULTI && col + 1 >= c_lo2 && col + 1 < c_hi2);
             pk[j] &= (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
           }
         }
@@ -651,16 +661,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool MULTI>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
                           int n_items, cudaStream_t stream) {
   using L = BwdLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(bda_bwd_dkdv_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(bda_bwd_dkdv_kernel<D, MULTI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::BYTES));
   if (e != cudaSuccess) return e;
   const unsigned grid = unsigned(n_items) * unsigned(a.hkv);
-  bda_bwd_dkdv_kernel<D><<<grid, kBwdThreads, L::BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
+  bda_bwd_dkdv_kernel<D, MULTI><<<grid, kBwdThreads, L::BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 
@@ -696,8 +706,12 @@ cudaError_t launch_bwd_dkdv(int head_dim, const CUtensorMap& tq, const CUtensorM
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                             const BwdArgs& a, int n_items, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
-  if (head_dim == 128) return launch_dkdv_t<128>(tq, tk, tv, tdo, tdq, a, n_items, stream);
-  return launch_dkdv_t<64>(tq, tk, tv, tdo, tdq, a, n_items, stream);
+  const bool multi = a.cgroups != nullptr;
+  if (head_dim == 128)
+    return multi ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, tdq, a, n_items, stream)
+                 : launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdq, a, n_items, stream);
+  return multi ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, tdq, a, n_items, stream)
+               : launch_dkdv_t<64, false>(tq, tk, tv, tdo, tdq, a, n_items, stream);
 }
 
 cudaError_t launch_dq_convert(int head_dim, const float* dq_acc, __nv_bfloat16* dq, int64_t total_q,

@@ -1,0 +1,548 @@
+// bda_decode.cu -- split forward for problems that fill few SMs (a decode
+// step), with bf16 or FP8 (e4m3) K/V.
+//
+// A decode step of a block-diffusion model attends one active block of 32
+// query tokens to the committed prefix plus the block itself (the
+// block-causal attention of the ORL announcement thread, 24vids.com mirror,
+// highlight 3, with the queries at the end of the keys).  Its forward has one
+// 128-row query tile per head group -- 8 units for 148 SMs -- so one CTA per
+// unit streams the whole KV cache through one SM.  Here the key tiles of a
+// query tile are cut into chunks (the plan's DecItems), one CTA per (chunk,
+// head group), and a combine kernel merges the chunks' partial results:
+// with LSE_s in log2 units,
+//   M = max_s LSE_s,  w_s = 2^(LSE_s - M),  O = sum_s w_s O_s / sum_s w_s,
+//   LSE = (M + log2 sum_s w_s) ln 2.
+// The combine kernel is launched as a programmatic dependent of the split
+// kernel, so its launch overlaps the split kernel and it waits on the device
+// for the split kernel's results.
+//
+// FP8 K/V (the engine of the ORL paper card runs its NVFP4 configurations
+// with an FP8 KV cache, Table 11 caption): K and V arrive as e4m3 codes with
+// one fp32 dequantisation scale per KV head (k = code * k_scale[h]).  The TMA
+// brings the codes into shared memory (half the HBM bytes of bf16); the
+// softmax warps expand them exactly to bf16 (every e4m3 value is a bf16
+// value) in the swizzled layout the MMA reads, and the scales are applied in
+// fp32: S = k_scale * (Q K8^T), O = v_scale * (P V8).
+//
+// Roles (192 threads): warps 0..3 expand FP8 tiles, run the softmax (thread r
+// owns TMEM lane r = query row r) and the epilogue; warp 4 issues the TMA
+// loads; warp 5 allocates TMEM and issues the MMAs (one thread).
+// TMEM columns: S [0,128)  O [128,128+D)  P [128+D,192+D).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bda_internal.h"
+#include "bda_kernels.h"
+#include "bda_ptx.cuh"
+
+namespace bda {
+namespace {
+
+constexpr int kDecThreads = 192;
+constexpr uint32_t kColS = 0, kColO = 128;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the persistent forward
+
+template <int D, bool KV8>
+struct DecLayout {
+  static constexpr int CH = D / 64;
+  static constexpr uint32_t CHUNK = 128 * 128;   // [128 rows][64 bf16], 128B-swizzled
+  static constexpr uint32_t TILE = CH * CHUNK;   // bf16 tile of 128 rows x D
+  static constexpr uint32_t TILE8 = 128 * D;     // e4m3 tile [128 keys][D bytes], unswizzled
+  static constexpr uint32_t Q = 0;
+  static constexpr uint32_t KB = Q + TILE;        // bf16 K, 2 stages
+  static constexpr uint32_t VB = KB + 2 * TILE;   // bf16 V, 2 stages
+  static constexpr uint32_t K8 = VB + 2 * TILE;   // e4m3 K, 2 stages (FP8 only)
+  static constexpr uint32_t V8 = K8 + (KV8 ? 2 * TILE8 : 0);
+  static constexpr uint32_t BAR = V8 + (KV8 ? 2 * TILE8 : 0);
+  enum {
+    B_Q = 0, B_KF = 1 /*[2]*/, B_VF = 3 /*[2]*/, B_KC = 5 /*[2]*/, B_VC = 7 /*[2]*/,
+    B_KE = 9 /*[2]*/, B_VE = 11 /*[2]*/, B_SF = 13, B_SFREE, B_PF, B_OD, B_DRAIN, NBAR
+  };
+  static constexpr uint32_t MISC = BAR + 8 * NBAR;
+  static constexpr uint32_t BYTES = MISC + 16;
+  static constexpr uint32_t ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
+  // TMEM: S [0,128), O [128,128+D), P [128+D,128+D+64); a power of two >= 32.
+  static constexpr uint32_t COL_P = kColO + D;
+  static constexpr uint32_t TMEM_COLS = D == 64 ? 256 : 512;
+};
+
+__device__ __forceinline__ bool drain_wait(WaitCtx w, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > w.timeout_ns) {
+      atomicOr(w.status, kDeviceTimeoutCode);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int w0) {
+  const int l = min(max(lo - w0, 0), 32), h = min(max(hi - w0, 0), 32);
+  if (h <= l) return 0u;
+  const uint32_t below_h = h == 32 ? 0xffffffffu : (1u << h) - 1u;
+  const uint32_t below_l = l == 32 ? 0xffffffffu : (1u << l) - 1u;
+  return below_h & ~below_l;
+}
+
+// Two e4m3 codes (low byte first) -> the same two values as a bf16 pair.
+// Exact: every e4m3 value is an f16 value, every f16 value from e4m3 has at
+// most 4 significant bits and fits bf16.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+  const float2 f = __half22float2(h);
+  return pack_bf16x2(f.x, f.y);
+}
+
+// Expands one e4m3 tile [128 keys][D bytes] into the bf16 swizzled layout the
+// MMA reads (CH chunks of [128 rows][128 B]); 128 threads, 16 codes each per
+// step.  Reads are contiguous across a warp; writes follow the swizzle.
+template <int D>
+__device__ __forceinline__ void expand_fp8_tile(const uint8_t* src, uint8_t* dst, int t) {
+  constexpr int UPR = D / 16;           // 16-byte units of codes per key row
+  constexpr int STEPS = 128 * UPR / 128;
+#pragma unroll
+  for (int i = 0; i < STEPS; ++i) {
+    const int q = i * 128 + t;
+    const int row = q / UPR, u = q % UPR;
+    const uint4 c = *reinterpret_cast<const uint4*>(src + row * D + u * 16);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t b[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      b[2 * k] = e4m3x2_to_bf16x2(uint16_t(w[k] & 0xffffu));
+      b[2 * k + 1] = e4m3x2_to_bf16x2(uint16_t(w[k] >> 16));
+    }
+    // codes 16u .. 16u+15 of the row = bf16 elements d0 .. d0+15
+    const int d0 = u * 16, ch = d0 >> 6, unit = (d0 & 63) >> 3;
+    uint8_t* base = dst + ch * (128 * 128);
+    *reinterpret_cast<uint4*>(base + sw128_offset(row, unit)) = make_uint4(b[0], b[1], b[2], b[3]);
+    *reinterpret_cast<uint4*>(base + sw128_offset(row, unit + 1)) =
+        make_uint4(b[4], b[5], b[6], b[7]);
+  }
+}
+
+template <int D, bool KV8>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    bda_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using L = DecLayout<D, KV8>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto bar = [&](int i) -> uint32_t { return base + L::BAR + 8u * uint32_t(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::MISC + 4);
+
+  // The combine kernel may start launching now; it waits on the device for
+  // this grid's completion before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  const int unit = blockIdx.x;
+  const int dec_idx = unit / a.n_groups;
+  const int grp = unit - dec_idx * a.n_groups;
+  const DecItem dj = a.dec[dec_idx];
+  const FwdItem it = a.items[dj.item];
+  const int head0 = grp * a.hg, kvh = head0 / a.G;
+  const int n = dj.kt_hi - dj.kt_lo;  // key tiles of this unit (>= 1)
+  auto key_tile = [&](int j) -> int {
+    const int m = dj.kt_lo + j;
+    return m < it.r1_end ? m : it.r2_begin + (m - it.r1_end);
+  };
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(L::B_Q), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::B_KF + s), 1);
+      mbar_init(bar(L::B_VF + s), 1);
+      mbar_init(bar(L::B_KC + s), 128);
+      mbar_init(bar(L::B_VC + s), 128);
+      mbar_init(bar(L::B_KE + s), 1);
+      mbar_init(bar(L::B_VE + s), 1);
+    }
+    mbar_init(bar(L::B_SF), 1);
+    mbar_init(bar(L::B_SFREE), 128);
+    mbar_init(bar(L::B_PF), 128);
+    mbar_init(bar(L::B_OD), 1);
+    mbar_init(bar(L::B_DRAIN), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  // Failure-detection testing: CTA 0 leaves its Q load un-issued and waits
+  // only fault_timeout_ns for it (a.fault is 0 in normal use).
+  const bool fault_cta = a.fault != 0 && blockIdx.x == 0;
+  const WaitCtx wc{abort_flag, a.status, fault_cta ? a.fault_timeout_ns : a.timeout_ns};
+  // A K/V stage is ready for the MMA once loaded (bf16) or expanded (FP8).
+  const int b_kready = KV8 ? L::B_KC : L::B_KF;
+  const int b_vready = KV8 ? L::B_VC : L::B_VF;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const bool q_issued = !fault_cta;
+      if (q_issued) {
+        mbar_arrive_expect_tx(bar(L::B_Q), L::TILE);
+        for (int c = 0; c < L::CH; ++c)
+          tma_load_3d(base + L::Q + c * L::CHUNK, &tm_q, bar(L::B_Q), c * 64, head0, it.q_row);
+      }
+      int nk[2] = {0, 0}, nv[2] = {0, 0};  // copies issued per stage (abort drain)
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        const int s = j & 1;
+        const uint32_t prev = uint32_t((j >> 1) - 1) & 1u;
+        const int krow = it.k_row + key_tile(j) * kTileN;
+        // The stage is free once its previous tile was consumed: expanded
+        // (FP8: the codes are read once) or read by the MMA (bf16).
+        const int b_kfree = KV8 ? L::B_KC : L::B_KE;
+        const int b_vfree = KV8 ? L::B_VC : L::B_VE;
+        if (j >= 2 && !mbar_wait(wc, bar(b_kfree + s), prev)) { ok = false; break; }
+        if (KV8) {
+          mbar_arrive_expect_tx(bar(L::B_KF + s), L::TILE8);
+          tma_load_3d(base + L::K8 + s * L::TILE8, &tm_k, bar(L::B_KF + s), 0, kvh, krow);
+        } else {
+          mbar_arrive_expect_tx(bar(L::B_KF + s), L::TILE);
+          for (int c = 0; c < L::CH; ++c)
+            tma_load_3d(base + L::KB + s * L::TILE + c * L::CHUNK, &tm_k, bar(L::B_KF + s), c * 64,
+                        kvh, krow);
+        }
+        ++nk[s];
+        if (j >= 2 && !mbar_wait(wc, bar(b_vfree + s), prev)) { ok = false; break; }
+        if (KV8) {
+          mbar_arrive_expect_tx(bar(L::B_VF + s), L::TILE8);
+          tma_load_3d(base + L::V8 + s * L::TILE8, &tm_v, bar(L::B_VF + s), 0, kvh, krow);
+        } else {
+          mbar_arrive_expect_tx(bar(L::B_VF + s), L::TILE);
+          for (int c = 0; c < L::CH; ++c)
+            tma_load_3d(base + L::VB + s * L::TILE + c * L::CHUNK, &tm_v, bar(L::B_VF + s), c * 64,
+                        kvh, krow);
+        }
+        ++nv[s];
+      }
+      {
+        // Every copy issued lands before the CTA can exit (at once on the
+        // normal path, where the consumers have waited for them already).
+        (void)ok;
+        if (q_issued) drain_wait(wc, bar(L::B_Q), 0);
+        for (int s = 0; s < 2; ++s) {
+          if (nk[s]) drain_wait(wc, bar(L::B_KF + s), uint32_t(nk[s] - 1) & 1u);
+          if (nv[s]) drain_wait(wc, bar(L::B_VF + s), uint32_t(nv[s] - 1) & 1u);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        const uint32_t ka = base + L::KB + s * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+          mma_ss(tbase + kColS, sdesc_sw128(base + L::Q + off, 16, 1024),
+                 sdesc_sw128(ka + off, 16, 1024), idS, kk > 0);
+        }
+        mma_commit(bar(L::B_SF));
+        mma_commit(bar(L::B_KE + s));
+      };
+      auto issue_pv = [&](int j) {
+        const int s = j & 1;
+        const uint32_t va = base + L::VB + s * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ts(tbase + kColO, tbase + L::COL_P + 8u * kk, sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024),
+                 idO, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::B_OD));
+        mma_commit(bar(L::B_VE + s));
+      };
+      bool go = mbar_wait(wc, bar(L::B_Q), 0);
+      // S(j) waits for its K and for the softmax to have read S(j-1); P V(j-1)
+      // is issued behind S(j), so the product overlaps the next softmax.
+      for (int j = 0; go && j < n; ++j) {
+        const int s = j & 1;
+        go = mbar_wait(wc, bar(b_kready + s), uint32_t(j >> 1) & 1u) &&
+             (j == 0 || mbar_wait(wc, bar(L::B_SFREE), uint32_t(j - 1) & 1u));
+        if (!go) break;
+        tc_fence_after();
+        issue_s(j);
+        if (j > 0) {
+          const int sp = (j - 1) & 1;
+          go = mbar_wait(wc, bar(L::B_PF), uint32_t(j - 1) & 1u) &&
+               mbar_wait(wc, bar(b_vready + sp), uint32_t((j - 1) >> 1) & 1u);
+          if (!go) break;
+          tc_fence_after();
+          issue_pv(j - 1);
+        }
+      }
+      if (go) {
+        const int jl = n - 1, sl = jl & 1;
+        go = mbar_wait(wc, bar(L::B_PF), uint32_t(jl) & 1u) &&
+             mbar_wait(wc, bar(b_vready + sl), uint32_t(jl >> 1) & 1u);
+        if (go) {
+          tc_fence_after();
+          issue_pv(jl);
+        }
+      }
+      // Every MMA issued above completes before TMEM can be released.
+      mma_commit(bar(L::B_DRAIN));
+      drain_wait(wc, bar(L::B_DRAIN), 0);
+    }
+  } else {
+    // ------------------------------------- FP8 expansion, softmax, epilogue
+    const int r = tid;  // TMEM lane == query row of the tile
+    const int t_local = r >> a.lg_hg;
+    const int hh = r & (a.hg - 1);
+    const bool row_valid = t_local < it.q_len;
+    const int p = it.pos0 + (row_valid ? t_local : it.q_len - 1);
+    const RowKeys rk = row_keys_g(p, it.prefix, a.block, it.lk, a.cgroups + it.grp_off, it.n_grp);
+    const uint32_t lane_addr = tbase + (uint32_t(warp * 32) << 16);
+    float sl2 = a.scale_log2;
+    float o_mul = 1.f;
+    if (KV8) {
+      sl2 *= a.k_scale[kvh];
+      o_mul = a.v_scale[kvh];
+    }
+    bool ok = true;
+    float m_ref = -INFINITY, l = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const int s = j & 1;
+      const uint32_t ph = uint32_t(j >> 1) & 1u, prev = uint32_t((j >> 1) - 1) & 1u;
+      if (KV8) {
+        // Expand K(j), then V(j): the codes have landed and the MMAs that
+        // read this bf16 stage two tiles ago have completed.
+        if (!mbar_wait_warp(wc, bar(L::B_KF + s), ph) ||
+            (j >= 2 && !mbar_wait_warp(wc, bar(L::B_KE + s), prev))) { ok = false; break; }
+        expand_fp8_tile<D>(gbase + L::K8 + s * L::TILE8, gbase + L::KB + s * L::TILE, r);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::B_KC + s));
+        if (!mbar_wait_warp(wc, bar(L::B_VF + s), ph) ||
+            (j >= 2 && !mbar_wait_warp(wc, bar(L::B_VE + s), prev))) { ok = false; break; }
+        expand_fp8_tile<D>(gbase + L::V8 + s * L::TILE8, gbase + L::VB + s * L::TILE, r);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::B_VC + s));
+      }
+      if (!mbar_wait_warp(wc, bar(L::B_SF), uint32_t(j) & 1u)) { ok = false; break; }
+      tc_fence_after();
+      float sv[kTileN];
+      {
+        uint32_t rr[kTileN / 32][32];
+#pragma unroll
+        for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(lane_addr + kColS + 32u * c, rr[c]);
+#pragma unroll
+        for (int c = 0; c < kTileN / 32; ++c) tmem_ld_wait(rr[c]);
+#pragma unroll
+        for (int c = 0; c < kTileN / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(rr[c][i]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::B_SFREE));
+      if (dj.kt_lo + j >= it.n_full) {  // PARTIAL tile: mask from block indices
+        const int k0 = key_tile(j) * kTileN;
+        const int ca = rk.a - k0, cb = rk.b - k0, ce = rk.e - k0;
+        uint32_t keep[kTileN / 32];
+#pragma unroll
+        for (int w = 0; w < kTileN / 32; ++w)
+          keep[w] = range_bits(0, ca, 32 * w) | range_bits(cb, ce, 32 * w);
+#pragma unroll
+        for (int i = 0; i < kTileN; ++i)
+          if (!(keep[i >> 5] & (1u << (i & 31)))) sv[i] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx8[q] = sv[q];
+#pragma unroll
+      for (int i = 8; i < kTileN; i += 8)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx8[q] = fmaxf(mx8[q], sv[i + q]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_cand = mx * sl2;
+      float alpha = 1.f;
+      if (m_cand > m_ref + kRescaleThreshold) {
+        alpha = ex2(m_ref - m_cand);  // 0 on the first finite max
+        m_ref = m_cand;
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // P(j) overwrites P(j-1): P V(j-1) must have completed (it also makes
+      // O complete for a rescale).
+      if (j > 0) {
+        if (!mbar_wait_warp(wc, bar(L::B_OD), uint32_t(j - 1) & 1u)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(lane_addr + kColO + 32u * c, rr);
+            tmem_ld_wait(rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(lane_addr + kColO + 32u * c, rr);
+          }
+        }
+      }
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < kTileN / 64; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(sv[64 * c + 2 * i], sl2, -m_use));
+          const float p1 = ex2(fmaf(sv[64 * c + 2 * i + 1], sl2, -m_use));
+          rs[i & 3] += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(lane_addr + L::COL_P + 32u * c, pk);
+      }
+      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::B_PF));
+    }
+    // Epilogue: O out of TMEM once the last P V has completed.
+    if (ok && mbar_wait_warp(wc, bar(L::B_OD), uint32_t(n - 1) & 1u)) {
+      tc_fence_after();
+      uint32_t ov[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_addr + kColO + 32u * c, ov[c]);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld_wait(ov[c]);
+      // A row that sees no key of this chunk (possible in a split) has l = 0:
+      // its partial is O = 0 with LSE = -inf, weight 0 in the combine.
+      const float inv_l = l > 0.f ? o_mul / l : 0.f;
+      const float lse2 = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+      if (row_valid && dj.part < 0) {
+        __nv_bfloat16* orow =
+            a.o + (size_t(it.q_row + t_local) * a.hq + size_t(head0 + hh)) * size_t(D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(ov[c][2 * i]) * inv_l,
+                                __uint_as_float(ov[c][2 * i + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+        a.lse[size_t(head0 + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
+            lse2 * 0.69314718055994530942f;
+      } else if (row_valid) {
+        // Partial of this chunk: normalised O (fp32, row-fastest so a warp's
+        // stores and the combine's loads are contiguous) and its log2 LSE.
+        const size_t slot = size_t(dj.part) * size_t(a.n_groups) + size_t(grp);
+        float* po = a.part_o + slot * size_t(D) * kTileM + r;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) po[size_t(32 * c + i) * kTileM] = __uint_as_float(ov[c][i]) * inv_l;
+        a.part_lse[slot * kTileM + r] = lse2;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, L::TMEM_COLS);
+  }
+}
+
+// Merges the chunks of every split query tile.  Block = (forward item, head
+// group, 16 of the D columns); thread r = tile row r, so for each chunk and
+// column a warp's loads are 32 consecutive floats.
+template <int D>
+__global__ void __launch_bounds__(kTileM) bda_fwd_combine_kernel(const FwdArgs a) {
+  // Wait for the split kernel (this grid may have launched while it ran).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int NSL = D / 16;
+  const int b = blockIdx.x;
+  const int sl = b % NSL, rest = b / NSL;
+  const int grp = rest % a.n_groups, item = rest / a.n_groups;
+  const FwdItem it = a.items[item];
+  if (it.n_split <= 1) return;
+  const int r = threadIdx.x, t_local = r >> a.lg_hg, hh = r & (a.hg - 1);
+  if (t_local >= it.q_len) return;
+  auto slot = [&](int s) -> size_t { return size_t(it.part0 + s) * size_t(a.n_groups) + size_t(grp); };
+  float M = -INFINITY;
+  for (int s = 0; s < it.n_split; ++s) M = fmaxf(M, a.part_lse[slot(s) * kTileM + r]);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  float Lsum = 0.f;
+  for (int s = 0; s < it.n_split; ++s) {
+    const float w = ex2(a.part_lse[slot(s) * kTileM + r] - M);
+    Lsum += w;
+    const float* ps = a.part_o + (slot(s) * size_t(D) + size_t(16 * sl)) * kTileM + r;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = fmaf(w, ps[size_t(i) * kTileM], acc[i]);
+  }
+  const float inv = 1.f / Lsum;
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+  __nv_bfloat16* orow =
+      a.o + (size_t(it.q_row + t_local) * a.hq + size_t(grp * a.hg + hh)) * size_t(D) + 16 * sl;
+  reinterpret_cast<uint4*>(orow)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  reinterpret_cast<uint4*>(orow)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  if (sl == 0)
+    a.lse[size_t(grp * a.hg + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
+        (M + log2f(Lsum)) * 0.69314718055994530942f;
+}
+
+template <int D, bool KV8>
+cudaError_t launch_decode_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdArgs& a, int n_dec, int n_items, bool combine,
+                            cudaStream_t stream) {
+  using L = DecLayout<D, KV8>;
+  static_assert(L::ALLOC <= 232448, "decode shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(bda_decode_kernel<D, KV8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::ALLOC));
+  if (e != cudaSuccess) return e;
+  const unsigned grid = unsigned(n_dec) * unsigned(a.n_groups);
+  bda_decode_kernel<D, KV8><<<grid, kDecThreads, L::ALLOC, stream>>>(tq, tk, tv, a);
+  if ((e = cudaGetLastError()) != cudaSuccess || !combine) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(n_items) * unsigned(a.n_groups) * unsigned(D / 16));
+  cfg.blockDim = dim3(kTileM);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bda_fwd_combine_kernel<D>, a);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(int head_dim, bool kv8, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const FwdArgs& a, int n_dec, int n_items,
+                          bool combine, cudaStream_t stream) {
+  if (n_dec == 0) return cudaSuccess;
+  if (head_dim == 128)
+    return kv8 ? launch_decode_t<128, true>(tq, tk, tv, a, n_dec, n_items, combine, stream)
+               : launch_decode_t<128, false>(tq, tk, tv, a, n_dec, n_items, combine, stream);
+  return kv8 ? launch_decode_t<64, true>(tq, tk, tv, a, n_dec, n_items, combine, stream)
+             : launch_decode_t<64, false>(tq, tk, tv, a, n_dec, n_items, combine, stream);
+}
+
+}  // namespace bda

@@ -20,7 +20,19 @@ struct Shape {
   int n_fwd = 0;    // forward work items (query tiles)
   int n_bwd = 0;    // backward work items (key tiles)
   int n_cgroups = 0;  // non-empty copy groups (multi-block staircase)
+  // Split (decode) forward, for problems that fill few SMs: key tiles per
+  // unit (0: no item is split), units, and partial-result slots.
+  int split_c = 0;
+  int n_dec = 0;
+  int n_parts = 0;
 };
+
+// A problem with fewer than kSplitMaxUnits forward units (query tile x head
+// group) fills under half of a B300's 148 SMs; its forward splits the key
+// tiles of each query tile into chunks of split_c tiles, split_c chosen so
+// the units number about kSplitTargetUnits.
+constexpr int kSplitMaxUnits = 74;
+constexpr int kSplitTargetUnits = 148;
 
 // Validates the problem and mask; fills `s`.  Host-only, launches nothing.
 // A multi-block staircase whose non-empty groups are not in block order
@@ -29,10 +41,16 @@ struct Shape {
 bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s,
                     bool count_only = false);
 
-// Plan bytes: header, forward items, (with_bwd) backward items, then the
-// copy-group table (int2 per non-empty group, padded to 16 bytes).
+// Plan bytes: header, forward items, (with_bwd) backward items, the
+// copy-group table (int2 per non-empty group, padded to 16 bytes), then the
+// split-forward units (DecItem each).
 size_t plan_bytes(const Shape& s, bool with_bwd = true);
 size_t plan_group_offset(const Shape& s, bool with_bwd);
+size_t plan_dec_offset(const Shape& s, bool with_bwd);
+// Workspace: the plan, then the split forward's partial results (fp32 O
+// [n_parts * n_groups][d][128] and log2 LSE [n_parts * n_groups][128]).
+size_t ws_offset_parts(const Shape& s);
+size_t ws_offset_part_lse(const Shape& s);
 size_t workspace_bytes(const Shape& s, bool with_bwd);
 size_t ws_offset_D(const Shape& s);      // fp32 [hq][total_q]
 size_t ws_offset_dqacc(const Shape& s);  // fp32 [total_q][hq][d]
@@ -57,5 +75,7 @@ bool make_thd_map(void* map, const void* ptr, int d, int heads, int64_t rows, in
 // heads x box_rows rows.
 bool make_f32_map(void* map, const void* ptr, int d, int heads, int64_t rows, int box_h,
                   int box_rows);
+// e4m3 codes [rows][heads][d]: box = d codes x 1 head x 128 rows, no swizzle.
+bool make_fp8_map(void* map, const void* ptr, int d, int heads, int64_t rows);
 
 }  // namespace bda

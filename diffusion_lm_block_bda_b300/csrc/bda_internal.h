@@ -55,9 +55,21 @@ struct FwdItem {
   int32_t seq;
   int32_t grp_off;   // the sequence's copy groups in the plan's table ...
   int32_t n_grp;     // ... (0: every copy sees the whole prefix)
-  int32_t pad[2];
+  int32_t n_split;   // split forward: key-tile chunks of this tile (1: none) ...
+  int32_t part0;     // ... and the first partial-result slot of its chunks
 };
 static_assert(sizeof(FwdItem) == 64, "FwdItem layout");
+
+// One unit of the split (decode) forward: key tiles [kt_lo, kt_hi) of the
+// tile list of forward item `item`; `part` is its partial-result slot, or -1
+// when the item is not split (the unit then writes O and LSE itself).
+struct DecItem {
+  int32_t item;
+  int32_t kt_lo;
+  int32_t kt_hi;
+  int32_t part;
+};
+static_assert(sizeof(DecItem) == 16, "DecItem layout");
 
 // One backward work unit: a 128-key tile of one sequence (all KV heads run it
 // in parallel); query tokens [q_begin, q_end) are the ones that see it.
@@ -91,6 +103,9 @@ struct PlanHeader {
   int32_t total_q;
   int32_t total_k;
   int32_t n_cgroups;  // entries of the copy-group table (after the items)
+  int32_t n_dec;      // split-forward units (after the copy-group table)
+  int32_t n_parts;    // partial-result slots of split forward items
+  int32_t split_c;    // key tiles per split-forward unit (0: no item is split)
 };
 
 // Keys visible to the query at position p: [0, a) U [b, e).

@@ -33,6 +33,14 @@ struct FwdArgs {
   // fault_timeout_ns and the CTA takes its abort path.
   int fault;
   uint64_t fault_timeout_ns;
+  // Split (decode) forward: its units, and the workspace's partial results
+  // (null when the plan splits no item).
+  const DecItem* dec;
+  float* part_o;    // [n_parts * n_groups][D][128] fp32, normalised O of a chunk
+  float* part_lse;  // [n_parts * n_groups][128] fp32, log2 LSE of a chunk
+  // FP8 K/V: per-KV-head dequantisation scales (device, fp32 [hkv]).
+  const float* k_scale;
+  const float* v_scale;
 };
 
 struct BwdArgs {
@@ -58,7 +66,7 @@ struct BwdArgs {
 // array) holding the items of `s` (with or without the backward items).
 // Consumes a failure-detection test fault armed for that stage, if any.
 FwdArgs make_fwd_args(const Shape& s, const uint8_t* plan, bool with_bwd, void* o, float* lse,
-                      uint32_t* status);
+                      uint32_t* status, uint8_t* ws_parts = nullptr);
 BwdArgs make_bwd_args(const Shape& s, const uint8_t* plan, const float* lse, const float* D,
                       void* dk, void* dv, uint32_t* status);
 
@@ -67,6 +75,20 @@ BwdArgs make_bwd_args(const Shape& s, const uint8_t* plan, const float* lse, con
 cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, int n_items,
                        cudaStream_t stream);
+
+// Split forward (one CTA per DecItem x head group; bf16 or e4m3 K/V) and,
+// when `combine`, the merge of split items' partial results, launched as a
+// programmatic dependent of the split kernel.
+cudaError_t launch_decode(int head_dim, bool kv8, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const FwdArgs& a, int n_dec, int n_items,
+                          bool combine, cudaStream_t stream);
+
+// e4m3 codes of x / scale[h] (bf16 [rows][heads][d] -> bytes, same layout).
+cudaError_t launch_quantize_fp8(const __nv_bfloat16* x, uint8_t* x8, const float* scale,
+                                int64_t rows, int heads, int d, cudaStream_t stream);
+// scale[h] = max |x[., h, .]| / 448 (1 for an all-zero head).
+cudaError_t launch_fp8_scales(const __nv_bfloat16* x, float* scale, int64_t rows, int heads, int d,
+                              cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(int head_dim, const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                   float* D, float* dq_acc, int64_t total_q, int hq,

@@ -36,6 +36,96 @@ int seq_prefix(const bda_mask_desc* m, int s, int lk) {
   return m->kind != BDA_MASK_BLOCK_CAUSAL ? m->prefix_len_host[s] : lk;
 }
 
+// The forward item of the query tile starting at local token t0 of sequence
+// sq: its key tiles [0, r1_end) and [r2_begin, r2_end), the first n_full of
+// them FULL.
+FwdItem make_fwd_item(const Shape& s, int sq, int q0, int lq, int k0, int lk, int P, int t0,
+                      int grp_off, int n_grp, const int2* grp) {
+  const int B = s.B;
+  FwdItem it{};
+  it.q_row = q0 + t0;
+  it.q_len = std::min(s.tok, lq - t0);
+  it.pos0 = t0 + (lk - lq);
+  it.k_row = k0;
+  it.lk = lk;
+  it.prefix = P;
+  it.seq = sq;
+  it.grp_off = grp_off;
+  it.n_grp = n_grp;
+  it.n_split = 1;
+  it.part0 = -1;
+  const int p_lo = it.pos0, p_hi = it.pos0 + it.q_len - 1;
+  // Rows see [0, a(p)) and their own copy.  Without copy groups a(p) grows
+  // with p; with them, take the extremes over the tile's rows.
+  int a_min, a_max;
+  if (n_grp == 0) {
+    a_min = row_keys(p_lo, P, B, lk).a;
+    a_max = row_keys(p_hi, P, B, lk).a;
+  } else {
+    a_min = lk;
+    a_max = 0;
+    for (int q = p_lo; q <= p_hi; ++q) {
+      const int a = row_keys_g(q, P, B, lk, grp, n_grp).a;
+      a_min = std::min(a_min, a);
+      a_max = std::max(a_max, a);
+    }
+  }
+  // Key tiles inside [0, a_min) are FULL for every row.
+  it.n_full = a_min / kTileN;
+  it.r1_end = ceil_div(a_max, kTileN);
+  it.r2_begin = it.r2_end = 0;
+  if (p_hi >= P) {  // copy rows: their own copies span [b(first copy row), e(p_hi))
+    const RowKeys c = row_keys(std::max(p_lo, P), P, B, lk);
+    const RowKeys hi = row_keys(p_hi, P, B, lk);
+    int b0 = c.b / kTileN, b1 = ceil_div(hi.e, kTileN);
+    if (b0 <= it.r1_end) {
+      it.r1_end = std::max(it.r1_end, b1);
+    } else {
+      it.r2_begin = b0;
+      it.r2_end = b1;
+    }
+  }
+  it.work = it.r1_end + (it.r2_end - it.r2_begin);
+  return it;
+}
+
+// Copy groups of sequence sq (non-empty only), as (first position, visible).
+int seq_groups(const bda_mask_desc* m, int sq, int P, int B, int2* out) {
+  int n = 0, start = P;
+  for (int g = m->group_offsets_host[sq]; g < m->group_offsets_host[sq + 1]; ++g) {
+    const int c = m->group_copies_host[g];
+    if (c == 0) continue;
+    out[n++] = int2{start, m->group_visible_host[g]};
+    start += c * B;
+  }
+  return n;
+}
+
+// Split chunk for a problem with few forward units: key tiles per unit so
+// that the units number about kSplitTargetUnits (0: no split).  Sums the
+// items' key-tile counts, so it builds them (only when few).
+int split_chunk(const bda_problem* p, const bda_mask_desc* m, const Shape& s) {
+  const int n_groups = s.hq / s.hg;
+  if (int64_t(s.n_fwd) * n_groups >= kSplitMaxUnits || s.n_fwd == 0) return 0;
+  std::vector<int2> grp(size_t(s.n_cgroups) + 1);
+  int64_t tiles = 0;
+  int max_work = 0;
+  for (int sq = 0; sq < s.nseq; ++sq) {
+    const int q0 = p->cu_seqlens_q_host[sq], lq = p->cu_seqlens_q_host[sq + 1] - q0;
+    const int k0 = p->cu_seqlens_k_host[sq], lk = p->cu_seqlens_k_host[sq + 1] - k0;
+    const int P = seq_prefix(m, sq, lk);
+    const int n_grp = s.kind == BDA_MASK_STAIRCASE_MULTI ? seq_groups(m, sq, P, s.B, grp.data()) : 0;
+    for (int t0 = 0; t0 < lq; t0 += s.tok) {
+      const FwdItem it = make_fwd_item(s, sq, q0, lq, k0, lk, P, t0, 0, n_grp, grp.data());
+      tiles += it.work;
+      max_work = std::max(max_work, it.work);
+    }
+  }
+  const int64_t units = tiles * n_groups;
+  const int c = int(std::max<int64_t>(1, (units + kSplitTargetUnits - 1) / kSplitTargetUnits));
+  return c < max_work ? c : 0;  // 0 when no item would be cut
+}
+
 }  // namespace
 
 bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s, bool count_only) {
@@ -117,6 +207,26 @@ bda_status validate(const bda_problem* p, const bda_mask_desc* m, Shape* s, bool
     r.n_fwd = int(nf);
     r.n_bwd = int(nb);
     r.n_cgroups = int(ng);
+    // Split forward: units and partial slots follow from the chunk size.
+    r.split_c = split_chunk(p, m, r);
+    r.n_dec = r.n_fwd;
+    r.n_parts = 0;
+    if (r.split_c > 0) {
+      std::vector<FwdItem> fw;
+      std::vector<int2> grp(size_t(r.n_cgroups) + 1);
+      r.n_dec = 0;
+      for (int i = 0; i < p->nseq; ++i) {
+        const int q0 = cq[i], lq = cq[i + 1] - q0, k0 = ck[i], lk = ck[i + 1] - k0;
+        const int P = seq_prefix(m, i, lk);
+        const int n_grp = multi ? seq_groups(m, i, P, r.B, grp.data()) : 0;
+        for (int t0 = 0; t0 < lq; t0 += r.tok) {
+          const int w = make_fwd_item(r, i, q0, lq, k0, lk, P, t0, 0, n_grp, grp.data()).work;
+          const int n_split = std::max(1, (w + r.split_c - 1) / r.split_c);
+          r.n_dec += n_split;
+          if (n_split > 1) r.n_parts += n_split;
+        }
+      }
+    }
     *s = r;
     // Groups out of block order are counted but not computed.
     return block_order || count_only ? BDA_OK : BDA_ERR_UNSUPPORTED;
@@ -130,18 +240,32 @@ size_t plan_group_offset(const Shape& s, bool with_bwd) {
          (with_bwd ? sizeof(BwdItem) * size_t(s.n_bwd) : 0);
 }
 
-size_t plan_bytes(const Shape& s, bool with_bwd) {
+size_t plan_dec_offset(const Shape& s, bool with_bwd) {
   return plan_group_offset(s, with_bwd) + ((sizeof(int2) * size_t(s.n_cgroups) + 15) & ~size_t(15));
 }
 
-size_t ws_offset_D(const Shape& s) { return align256(plan_bytes(s)); }
+size_t plan_bytes(const Shape& s, bool with_bwd) {
+  return plan_dec_offset(s, with_bwd) + sizeof(DecItem) * size_t(s.n_dec);
+}
+
+size_t ws_offset_parts(const Shape& s) { return align256(plan_bytes(s)); }
+
+size_t ws_offset_part_lse(const Shape& s) {
+  const size_t slots = size_t(s.n_parts) * size_t(s.hq / s.hg);
+  return ws_offset_parts(s) + align256(sizeof(float) * slots * size_t(s.d) * kTileM);
+}
+
+size_t ws_offset_D(const Shape& s) {
+  const size_t slots = size_t(s.n_parts) * size_t(s.hq / s.hg);
+  return ws_offset_part_lse(s) + align256(sizeof(float) * slots * kTileM);
+}
 
 size_t ws_offset_dqacc(const Shape& s) {
   return ws_offset_D(s) + align256(sizeof(float) * size_t(s.hq) * size_t(s.total_q));
 }
 
 size_t workspace_bytes(const Shape& s, bool with_bwd) {
-  if (!with_bwd) return align256(plan_bytes(s));
+  if (!with_bwd) return ws_offset_D(s);
   return ws_offset_dqacc(s) +
          align256(sizeof(float) * size_t(s.total_q) * size_t(s.hq) * size_t(s.d));
 }
@@ -159,6 +283,9 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
   h->total_q = int32_t(s.total_q);
   h->total_k = int32_t(s.total_k);
   h->n_cgroups = s.n_cgroups;
+  h->n_dec = s.n_dec;
+  h->n_parts = s.n_parts;
+  h->split_c = s.split_c;
   std::vector<FwdItem> fw;
   std::vector<BwdItem> bw;
   fw.reserve(s.n_fwd);
@@ -175,63 +302,12 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
     const int P = seq_prefix(m, sq, lk);
     const int delta = lk - lq;
     const int grp_off = n_table;
-    if (multi) {
-      int start = P;
-      for (int g = m->group_offsets_host[sq]; g < m->group_offsets_host[sq + 1]; ++g) {
-        const int c = m->group_copies_host[g];
-        if (c == 0) continue;
-        table[n_table++] = int2{start, m->group_visible_host[g]};
-        start += c * B;
-      }
-    }
+    if (multi) n_table += seq_groups(m, sq, P, B, table + n_table);
     const int n_grp = n_table - grp_off;
     const int2* grp = table + grp_off;
     // forward: query tiles of tok tokens
-    for (int t0 = 0; t0 < lq; t0 += s.tok) {
-      FwdItem it{};
-      it.q_row = q0 + t0;
-      it.q_len = std::min(s.tok, lq - t0);
-      it.pos0 = t0 + delta;
-      it.k_row = k0;
-      it.lk = lk;
-      it.prefix = P;
-      it.seq = sq;
-      it.grp_off = grp_off;
-      it.n_grp = n_grp;
-      const int p_lo = it.pos0, p_hi = it.pos0 + it.q_len - 1;
-      // Rows see [0, a(p)) and their own copy.  Without copy groups a(p)
-      // grows with p; with them, take the extremes over the tile's rows.
-      int a_min, a_max;
-      if (n_grp == 0) {
-        a_min = row_keys(p_lo, P, B, lk).a;
-        a_max = row_keys(p_hi, P, B, lk).a;
-      } else {
-        a_min = lk;
-        a_max = 0;
-        for (int q = p_lo; q <= p_hi; ++q) {
-          const int a = row_keys_g(q, P, B, lk, grp, n_grp).a;
-          a_min = std::min(a_min, a);
-          a_max = std::max(a_max, a);
-        }
-      }
-      // Key tiles inside [0, a_min) are FULL for every row.
-      it.n_full = a_min / kTileN;
-      it.r1_end = ceil_div(a_max, kTileN);
-      it.r2_begin = it.r2_end = 0;
-      if (p_hi >= P) {  // copy rows: their own copies span [b(first copy row), e(p_hi))
-        const RowKeys c = row_keys(std::max(p_lo, P), P, B, lk);
-        const RowKeys hi = row_keys(p_hi, P, B, lk);
-        int b0 = c.b / kTileN, b1 = ceil_div(hi.e, kTileN);
-        if (b0 <= it.r1_end) {
-          it.r1_end = std::max(it.r1_end, b1);
-        } else {
-          it.r2_begin = b0;
-          it.r2_end = b1;
-        }
-      }
-      it.work = it.r1_end + (it.r2_end - it.r2_begin);
-      fw.push_back(it);
-    }
+    for (int t0 = 0; t0 < lq; t0 += s.tok)
+      fw.push_back(make_fwd_item(s, sq, q0, lq, k0, lk, P, t0, grp_off, n_grp, grp));
     // backward: key tiles of 128 keys
     for (int kp = 0; with_bwd && kp < lk; kp += kTileN) {
       BwdItem it{};
@@ -294,6 +370,23 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
     }
     return a.work > b.work;
   });
+  // Split-forward units, in the forward items' (longest-first) order: each
+  // item's key tiles cut into n_split nearly equal chunks of about split_c.
+  DecItem* dec = reinterpret_cast<DecItem*>(out + plan_dec_offset(s, with_bwd));
+  int n_dec = 0, n_parts = 0;
+  for (size_t i = 0; i < fw.size(); ++i) {
+    FwdItem& it = fw[i];
+    it.n_split = s.split_c > 0 ? std::max(1, ceil_div(it.work, s.split_c)) : 1;
+    it.part0 = it.n_split > 1 ? n_parts : -1;
+    for (int c = 0; c < it.n_split; ++c) {
+      DecItem& d = dec[n_dec++];
+      d.item = int32_t(i);
+      d.kt_lo = int32_t(int64_t(c) * it.work / it.n_split);
+      d.kt_hi = int32_t(int64_t(c + 1) * it.work / it.n_split);
+      d.part = it.n_split > 1 ? n_parts + c : -1;
+    }
+    if (it.n_split > 1) n_parts += it.n_split;
+  }
   std::memcpy(out + kHeaderBytes, fw.data(), sizeof(FwdItem) * fw.size());
   std::memcpy(out + kHeaderBytes + sizeof(FwdItem) * fw.size(), bw.data(),
               sizeof(BwdItem) * bw.size());

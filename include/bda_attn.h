@@ -117,7 +117,8 @@ typedef struct {
 size_t bda_attn_plan_size(const bda_problem *prob, const bda_mask_desc *mask);
 
 /* Bytes of device workspace for fwd (with_bwd = 0) or fwd+bwd (with_bwd = 1):
- * the plan, a status word, and for the backward D = rowsum(dO*O) fp32
+ * the plan, a status word, the split forward's partial results (problems
+ * that fill few SMs), and for the backward D = rowsum(dO*O) fp32
  * [hq][total_q] plus an fp32 dQ accumulator [total_q][hq][head_dim].
  * 0 on invalid input. */
 size_t bda_attn_workspace_size(const bda_problem *prob, const bda_mask_desc *mask, int with_bwd);
@@ -143,10 +144,46 @@ bda_status bda_attn_plan_host(const bda_problem *prob, const bda_mask_desc *mask
                               size_t host_plan_bytes);
 
 /* Forward: o = softmax(scale * q k^T + mask) v and lse (natural log, fp32).
- * Rows of o/lse outside every sequence are not written. */
+ * Rows of o/lse outside every sequence are not written.  A problem whose
+ * query tiles fill few SMs (fewer than 74 tiles x head groups, e.g. a decode
+ * step) runs the split forward: each query tile's key tiles are cut into
+ * chunks, one CTA per chunk and head group, and a second kernel merges the
+ * chunks' partial results (kept in the workspace); larger problems run the
+ * persistent forward. */
 bda_status bda_attn_fwd(const bda_problem *prob, const bda_mask_desc *mask, const void *q,
                         const void *k, const void *v, void *o, float *lse, void *ws,
                         size_t ws_bytes, bda_stream_t stream);
+
+/* Forward with an FP8 KV cache (the decode engine of the ORL paper card runs
+ * its NVFP4 configurations with an FP8 KV cache, Table 11 caption).  k8, v8:
+ * e4m3 codes (OCP FP8 E4M3: bias 7, largest finite 448), one byte each,
+ * layout [total_k][hkv][head_dim]; k_scale, v_scale: DEVICE fp32 [hkv]
+ * dequantisation scales, K = k8 * k_scale[h], V = v8 * v_scale[h].  Computes
+ * the attention of bda_attn_fwd over those K and V: the codes are expanded
+ * exactly to bf16 in shared memory and the scales applied in fp32, so only
+ * the KV bytes read from HBM change.  Same plan and workspace as
+ * bda_attn_fwd (bda_attn_plan first); runs the split forward kernel for
+ * every problem size. */
+bda_status bda_attn_fwd_fp8kv(const bda_problem *prob, const bda_mask_desc *mask, const void *q,
+                              const void *k8, const void *v8, const float *k_scale,
+                              const float *v_scale, void *o, float *lse, void *ws, size_t ws_bytes,
+                              bda_stream_t stream);
+
+/* FP8 KV-cache quantisation (same source as bda_attn_fwd_fp8kv): x8 =
+ * e4m3(x / scale[h]) for bf16 x [rows][heads][head_dim] (DEVICE), bytes out
+ * in the same layout; the quotient is the IEEE fp32 division, rounded to
+ * the nearest e4m3 value with ties to even and saturated to +-448 (NaN stays
+ * NaN).  scale: DEVICE fp32 [heads].  head_dim 64 or 128; x and x8 16-byte
+ * aligned. */
+bda_status bda_kv_quantize_fp8(const void *x, void *x8, const float *scale, long long rows,
+                               int heads, int head_dim, bda_stream_t stream);
+
+/* Per-head dequantisation scales for bda_kv_quantize_fp8: scale[h] =
+ * max |x[., h, .]| / 448 (1 for a head that is all zero), so the largest
+ * value maps to the largest e4m3 code.  scale: DEVICE fp32 [heads],
+ * heads <= 4096. */
+bda_status bda_kv_fp8_scales(const void *x, float *scale, long long rows, int heads, int head_dim,
+                             bda_stream_t stream);
 
 /* Backward of sum(o * dout): dq, dk, dv (bf16, same layouts as q, k, v);
  * dk/dv sum over the query heads that share a KV head.  Needs o and lse from
@@ -229,6 +266,13 @@ bda_status bda_attn_fwd_noalloc_check_status(bda_stream_t stream);
  * launch are unspecified.  stage 0 disarms.  BDA_ERR_INVALID_ARG otherwise.
  * Never armed unless called. */
 bda_status bda_testing_arm_wait_timeout(int stage, unsigned long long timeout_ns);
+
+/* Testing hook (no counterpart on the pages): which forward kernel
+ * bda_attn_fwd runs -- 0 as the plan says (default), 1 always the
+ * persistent kernel, 2 always the split kernel.  Both compute the same
+ * result; tests use this to check each on every problem shape.
+ * BDA_ERR_INVALID_ARG for other values. */
+bda_status bda_testing_force_forward_kernel(int which);
 
 const char *bda_status_string(bda_status s);
 

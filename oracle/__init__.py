@@ -66,6 +66,11 @@ def _load():
         lib.oracle_bwd_seq_multi.argtypes = grp + [c_int, c_int, c_int, c_dbl, pd, pd, pd, pd,
                                                    c_int, c_int, pi, c_int, pi, c_int, pd, pd, pd]
         lib.oracle_bwd_seq_multi.restype = None
+        pu8 = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_e4m3_encode_array.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_long, pu8]
+        lib.oracle_e4m3_encode_array.restype = None
+        lib.oracle_e4m3_decode_array.argtypes = [pu8, ctypes.c_long, pd]
+        lib.oracle_e4m3_decode_array.restype = None
         _lib = lib
     return _lib
 
@@ -288,3 +293,40 @@ def count_pairs_packed(kind, B, cu_q, cu_k, prefix, groups=None) -> int:
         else:
             n += count_pairs(kind, B, _prefix(kind, prefix, s, Lk), Lq, Lk)
     return n
+
+
+# ------------------------------------------------------------ FP8 (e4m3)
+# The KV-cache format of the decode engine on the ORL paper card (Table 11
+# caption: NVFP4 configurations use an FP8 KV cache).  oracle.c holds the
+# OCP E4M3 definition: encode = round to nearest, ties to even, saturating
+# at 448; decode = the exact value of a code.
+
+def e4m3_encode(x) -> np.ndarray:
+    """fp32 values (any array-like; converted to float32 first) -> uint8 codes."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).ravel()
+    out = np.zeros(a.size, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(a.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), a.size,
+                                     _ptr(out, ctypes.c_uint8))
+    return out.reshape(np.shape(x))
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """uint8 codes -> fp64 values (NaN for the NaN codes)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8)).ravel()
+    out = np.zeros(c.size, dtype=np.float64)
+    _load().oracle_e4m3_decode_array(_ptr(c, ctypes.c_uint8), c.size, _ptr(out))
+    return out.reshape(np.shape(codes))
+
+
+def quantize_kv_e4m3(x, scale) -> np.ndarray:
+    """Codes of the FP8 KV cache: e4m3(fl32(x / scale[h])) for x [rows][heads][d]
+    (bf16 or fp32 values) and fp32 scales [heads]; the quotient is the IEEE
+    fp32 division."""
+    xf = np.asarray(_f64(x), dtype=np.float32)
+    s = np.asarray(scale, dtype=np.float32).reshape(1, -1, 1)
+    return e4m3_encode(xf / s)
+
+
+def dequantize_kv_e4m3(codes, scale) -> np.ndarray:
+    """fp64 values code * scale[h] of an FP8 KV cache [rows][heads][d]."""
+    return e4m3_decode(codes) * np.asarray(scale, dtype=np.float64).reshape(1, -1, 1)

@@ -395,3 +395,61 @@ void oracle_bwd_seq_multi(int B, int P, int n_groups, const int32_t *copies,
     bwd_seq_m(&mk, L, L, Hq, Hkv, d, scale, Q, K, V, dO, kvh_lo, kvh_hi, qrows, nq, krows, nk, dQ,
               dK, dV);
 }
+
+/* ------------------------------------------------------------------------
+ * FP8 E4M3 (OCP 8-bit floating point, E4M3 variant), the KV-cache format of
+ * the decode engine on the ORL paper card (Table 11 caption: the NVFP4
+ * configurations use an FP8 KV cache).  Bit layout s eeee mmm, exponent bias
+ * 7; exponent field 0 holds the subnormals m * 2^-9; field 1..15 holds
+ * (1 + m/8) * 2^(e-7), except s 1111 111, which is NaN; there are no
+ * infinities, so the largest finite magnitude is 1.75 * 2^8 = 448.
+ * Quantising a value: round to the nearest representable magnitude, ties to
+ * the even code; a magnitude that rounds above 448 saturates to 448; NaN
+ * stays NaN.
+ * ---------------------------------------------------------------------- */
+double oracle_e4m3_decode(unsigned char c)
+{
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+unsigned char oracle_e4m3_encode(float x)
+{
+    const unsigned char sign = signbit(x) ? 0x80 : 0x00;
+    if (isnan(x)) return (unsigned char)(sign | 0x7F);
+    const double a = fabs((double)x);
+    /* spacing of the representable magnitudes around a: 2^-9 below 2^-6
+     * (subnormals and the first binade), else 2^(floor(log2 a) - 3) */
+    double q;
+    if (a < ldexp(1.0, -6)) {
+        q = ldexp(1.0, -9);
+    } else {
+        int ex;
+        frexp(a, &ex); /* a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1 */
+        q = ldexp(1.0, ex - 1 - 3);
+    }
+    /* a / q is exact (q is a power of two); rint rounds ties to even */
+    double v = rint(a / q) * q;
+    if (v > 448.0) v = 448.0;
+    if (v == 0.0) return sign;
+    if (v < ldexp(1.0, -6)) return (unsigned char)(sign | (int)(v / ldexp(1.0, -9)));
+    int ex;
+    frexp(v, &ex);
+    const int e = ex - 1 + 7;                             /* biased exponent */
+    const int m = (int)((v / ldexp(1.0, ex - 1) - 1.0) * 8.0); /* exact */
+    return (unsigned char)(sign | (e << 3) | m);
+}
+
+void oracle_e4m3_encode_array(const float *x, long n, unsigned char *out)
+{
+    for (long i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(const unsigned char *c, long n, double *out)
+{
+    for (long i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
+}

@@ -72,24 +72,41 @@ def gpu_run(w, inputs, with_bwd=True, device="cuda"):
     return {n: t.float().cpu() for n, t in out.items()}
 
 
-def compare_full(w, inputs, got, with_bwd=True, kv_heads=None):
-    """Full oracle over every sequence (small workloads)."""
+def oracle_full(w, inputs, with_bwd=True, kv_heads=None):
+    """The fp64 oracle's outputs for a whole (small) workload."""
     heads = None
     G = w.hq // w.hkv
     if kv_heads is not None:
         heads = (kv_heads[0] * G, kv_heads[1] * G)
-    O, LSE = oracle.fwd(w.kind, w.block_size, w.cu_seqlens_q, w.cu_seqlens_k, w.prefix,
-                        inputs["q"], inputs["k"], inputs["v"], w.hq, w.hkv, w.softmax_scale,
-                        heads=heads, groups=w.groups)
+    ref = {}
+    ref["o"], ref["lse"] = oracle.fwd(w.kind, w.block_size, w.cu_seqlens_q, w.cu_seqlens_k,
+                                      w.prefix, inputs["q"], inputs["k"], inputs["v"], w.hq,
+                                      w.hkv, w.softmax_scale, heads=heads, groups=w.groups)
+    if with_bwd:
+        ref["dq"], ref["dk"], ref["dv"] = oracle.bwd(
+            w.kind, w.block_size, w.cu_seqlens_q, w.cu_seqlens_k, w.prefix, inputs["q"],
+            inputs["k"], inputs["v"], inputs["dout"], w.hq, w.hkv, w.softmax_scale,
+            kv_heads=kv_heads, groups=w.groups)
+    return ref
+
+
+def compare_full(w, inputs, got, with_bwd=True, kv_heads=None, ref=None):
+    """Full oracle over every sequence (small workloads); `ref` reuses an
+    oracle_full result."""
+    heads = None
+    G = w.hq // w.hkv
+    if kv_heads is not None:
+        heads = (kv_heads[0] * G, kv_heads[1] * G)
+    if ref is None:
+        ref = oracle_full(w, inputs, with_bwd, kv_heads)
+    O, LSE = ref["o"], ref["lse"]
     hs = slice(None) if heads is None else slice(*heads)
     ks = slice(None) if kv_heads is None else slice(*kv_heads)
     res = {}
     res["o"] = check_o(got["o"][:, hs].numpy(), O[:, hs], w.name)
     res["lse"] = check_lse(got["lse"][hs].numpy(), LSE[hs], w.name)
     if with_bwd:
-        dQ, dK, dV = oracle.bwd(w.kind, w.block_size, w.cu_seqlens_q, w.cu_seqlens_k, w.prefix,
-                                inputs["q"], inputs["k"], inputs["v"], inputs["dout"], w.hq,
-                                w.hkv, w.softmax_scale, kv_heads=kv_heads, groups=w.groups)
+        dQ, dK, dV = ref["dq"], ref["dk"], ref["dv"]
         res["dq"] = check_grad(got["dq"][:, hs].numpy(), dQ[:, hs], "dQ", w.name)
         res["dk"] = check_grad(got["dk"][:, ks].numpy(), dK[:, ks], "dK", w.name)
         res["dv"] = check_grad(got["dv"][:, ks].numpy(), dV[:, ks], "dV", w.name)

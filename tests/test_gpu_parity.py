@@ -13,7 +13,7 @@ import torch
 
 from diffusion_lm_block_bda_b300 import workloads as W
 
-from _parity import (check_sum_rules, compare_full, compare_sampled, gpu_run)
+from _parity import (check_sum_rules, compare_full, compare_sampled, gpu_run, oracle_full)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,10 +34,25 @@ def test_tiny_block_causal_c1():
 
 
 def test_decode_step_c2():
+    """The decode step takes the split forward (17 key tiles x 8 head groups
+    as 136 CTAs, merged by the combine kernel); the persistent forward must
+    agree with the oracle too."""
+    import diffusion_lm_block_bda_b300 as bda
+    from diffusion_lm_block_bda_b300 import Problem
     w = W.named("c2")
+    pb = Problem.from_workload(w)
+    buf = torch.zeros(bda.bda_attn_plan_size(pb), dtype=torch.uint8)
+    bda.bda_attn_plan_host(pb, buf)
+    hdr = buf[:64].numpy().view(np.int32)
+    assert hdr[11] == 1 and hdr[9] == 17 and hdr[10] == 17  # split_c, n_dec, n_parts
     inp = W.make_inputs(w, seed=0)
-    got = gpu_run(w, inp, with_bwd=False)
-    compare_full(w, inp, got, with_bwd=False)
+    ref = oracle_full(w, inp, with_bwd=False)
+    compare_full(w, inp, gpu_run(w, inp, with_bwd=False), with_bwd=False, ref=ref)
+    try:
+        bda.bda_testing_force_forward_kernel(1)
+        compare_full(w, inp, gpu_run(w, inp, with_bwd=False), with_bwd=False, ref=ref)
+    finally:
+        bda.bda_testing_force_forward_kernel(0)
 
 
 EDGE = [
@@ -59,11 +74,21 @@ EDGE = [
 
 @pytest.mark.parametrize("case", EDGE, ids=[f"e{i}" for i in range(len(EDGE))])
 def test_edge_cases_full_oracle(case):
+    """Every edge case through both forward kernels -- the persistent one and
+    the split one (which small problems take by default) -- and the backward,
+    each against the same oracle result."""
+    import diffusion_lm_block_bda_b300 as bda
     kind, B, hq, hkv, d, lq, lk, prefix = case
     w = W.custom(kind, B, hq, hkv, d, lq, lk, prefix, name=f"edge_{kind}_{B}_{hq}_{hkv}_{d}")
     inp = W.make_inputs(w, seed=3)
-    got = gpu_run(w, inp)
-    compare_full(w, inp, got)
+    ref = oracle_full(w, inp)
+    try:
+        for which in (1, 2):
+            assert bda.bda_testing_force_forward_kernel(which) == bda.BDA_OK
+            got = gpu_run(w, inp)
+            compare_full(w, inp, got, ref=ref)
+    finally:
+        bda.bda_testing_force_forward_kernel(0)
 
 
 def _align256(n):

@@ -22,7 +22,7 @@ from diffusion_lm_block_bda_b300 import Problem, workloads as W
 HDR = 256
 ITEM_INTS = 16
 FWD_FIELDS = ["q_row", "q_len", "pos0", "k_row", "lk", "prefix", "n_full", "r1_end", "r2_begin",
-              "r2_end", "work", "seq", "grp_off", "n_grp"]
+              "r2_end", "work", "seq", "grp_off", "n_grp", "n_split", "part0"]
 BWD_FIELDS = ["k_row", "k_len", "kpos0", "q_row", "lq", "lk", "prefix", "q_begin", "q_end",
               "q2_begin", "q2_end", "n_tiles1", "work", "seq", "grp_off", "n_grp"]
 
@@ -38,12 +38,41 @@ def decode(pb):
     items = a[HDR // 4:HDR // 4 + n_items * ITEM_INTS].reshape(-1, ITEM_INTS)
     fw = [dict(zip(FWD_FIELDS, map(int, r))) for r in items[:n_fwd]]
     bw = [dict(zip(BWD_FIELDS, map(int, r))) for r in items[n_fwd:n_fwd + n_bwd]]
-    n_cg = int(hdr[8])
+    n_cg, n_dec, n_parts, split_c = int(hdr[8]), int(hdr[9]), int(hdr[10]), int(hdr[11])
     table = a[HDR // 4 + n_items * ITEM_INTS:][:2 * n_cg].reshape(-1, 2)
-    assert a.size * 4 == HDR + 64 * n_items + -(-8 * n_cg // 16) * 16
+    table_words = -(-8 * n_cg // 16) * 4
+    assert a.size * 4 == HDR + 64 * n_items + 4 * table_words + 16 * n_dec
+    dec = a[HDR // 4 + n_items * ITEM_INTS + table_words:].reshape(-1, 4)
+    assert dec.shape[0] == n_dec
     for it in fw + bw:
         it["groups"] = [tuple(map(int, r)) for r in table[it["grp_off"]:it["grp_off"] + it["n_grp"]]]
+    check_split(fw, dec, n_parts, split_c)
     return fw, bw, hg, tok
+
+
+def check_split(fw, dec, n_parts, split_c):
+    """Split-forward units: each item's chunks cover its key tiles [0, work)
+    in order, each chunk non-empty and at most split_c + 1 tiles; partial
+    slots are numbered consecutively over the split items."""
+    by_item = {}
+    for item, lo, hi, part in dec.tolist():
+        by_item.setdefault(item, []).append((lo, hi, part))
+    assert sorted(by_item) == list(range(len(fw)))
+    next_part = 0
+    for i, it in enumerate(fw):
+        chunks = by_item[i]
+        assert len(chunks) == it["n_split"]
+        assert chunks[0][0] == 0 and chunks[-1][1] == it["work"]
+        assert all(a[1] == b[0] for a, b in zip(chunks, chunks[1:]))
+        assert all(hi > lo for lo, hi, _ in chunks)
+        if it["n_split"] > 1:
+            assert split_c > 0 and all(hi - lo <= split_c + 1 for lo, hi, _ in chunks)
+            assert it["part0"] == next_part
+            assert [p for _, _, p in chunks] == list(range(next_part, next_part + it["n_split"]))
+            next_part += it["n_split"]
+        else:
+            assert chunks[0][2] == -1 and it["part0"] == -1
+    assert next_part == n_parts
 
 
 def key_tiles(it):
@@ -207,6 +236,23 @@ def test_planner_named_workloads(name):
         assert copy_items and all(it["n_full"] == 8 and it["work"] == 9 for it in copy_items)
     if name == "c2":
         assert len(fw) == 1 and fw[0]["work"] == 17 and fw[0]["n_full"] == 16
+
+
+def test_split_forward_plans():
+    """Problems with fewer than 74 query-tile units split their key tiles so
+    the units number about 148; larger ones are not split."""
+    def header(pb):
+        buf = torch.zeros(bda.bda_attn_plan_size(pb), dtype=torch.uint8)
+        bda.bda_attn_plan_host(pb, buf)
+        h = buf[:64].numpy().view(np.int32)
+        return int(h[9]), int(h[10]), int(h[11])  # n_dec, n_parts, split_c
+    c2 = Problem.from_workload(W.named("c2"))
+    assert header(c2) == (17, 17, 1)  # 17 key tiles x 8 head groups = 136 units
+    long_decode = Problem([0, 32], [0, 32 * 1024], 32, 8, 128, W.BLOCK_CAUSAL, 32)
+    n_dec, n_parts, c = header(long_decode)  # 256 tiles x 8 groups: chunks of 14
+    assert c == 14 and n_dec == n_parts == 19
+    assert header(Problem.from_workload(W.named("c3")))[2] == 0
+    check_plan(W.custom(W.BLOCK_CAUSAL, 32, 32, 8, 128, [32, 32, 5], [2080, 700, 133]))
 
 
 def test_planner_long_sequence_counts():
