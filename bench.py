@@ -320,8 +320,8 @@ def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
     """The decode step (32 new queries over a 2,080-key context: 2,048
     committed tokens + the active block; Hq=32, Hkv=8, d=128; forward only)
     is bound by HBM bandwidth and latency, not by the tensor cores.  Its
-    forward runs the split kernel (each query tile's 17 key tiles as 136
-    CTAs) and the combine kernel.  As in a denoising loop, where every
+    forward runs the split kernel (each query tile's 17 key tiles as 9 chunks,
+    x 8 head groups = 72 CTAs) and the combine kernel.  As in a denoising loop, where every
     layer's KV cache has left L2 by the time the layer comes round again
     while the kernels' code stays cached, the timed launches rotate through 16
     copies of Q, K and V (144 MB, more than L2): each launch reads its copy
@@ -402,7 +402,7 @@ def decode_measurement(bda, dev, stream, hbm_gbs, reps=32, n_rot=16):
     achieved8 = nbytes8 / (us8 * 1e-6) / 1e9
     return {"workload": "decode step: 32 queries over 2,080 keys (2,048 + one block of 32), "
                         "Hq=32, Hkv=8, d=128, forward only",
-            "kernels": "split forward (17 key tiles x 8 head groups = 136 CTAs) + combine",
+            "kernels": "split forward (9 chunks of <= 2 key tiles x 8 head groups = 72 CTAs) + combine",
             "bound": "hbm", "bytes": nbytes, "us": us, "achieved": achieved,
             "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
             "l2": f"launches rotate through {n_rot} Q/K/V copies (> L2)",

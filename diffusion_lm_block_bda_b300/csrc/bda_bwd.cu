@@ -21,17 +21,28 @@
 //      and a second warpgroup moves the dQ partial TMEM -> smem, from where
 //      the TMA adds it into the fp32 accumulator (bulk tensor reduce-add).
 //   3. dq_convert: dQ = bf16(scale * accumulator).
-// Roles of the dK/dV kernel (352 threads):
-//   warps 0..3   softmax: P^T and dS^T, then the dK epilogue
-//   warps 4..7   dQ readout + staging for the TMA reduce, then the dV epilogue
-//   warp 8       producer: K/V once, then Q, dO (TMA) and LSE, D per query tile
-//   warp 9       MMA issuer (one thread)
-//   warp 10      waits on the MMAs' dependencies and gates warp 9
+// Roles of the dK/dV kernel (512 threads, four warpgroups):
+//   warps 0..3   softmax, query columns [0, 64) of each tile: P^T and dS^T,
+//                then the dK epilogue
+//   warps 4..7   softmax, query columns [64, 128), then the dV epilogue
+//   warps 8..11  dQ readout + staging for the TMA reduce
+//   warp 12      producer: K/V once, then Q, dO (TMA) and LSE, D per query tile
+//   warp 13      MMA issuer (one thread)
+//   warp 14      waits on the MMAs' dependencies and gates warp 13
+//   warp 15      idle
+// P and dS are elementwise in (key, query) given LSE and D, so the two
+// softmax warpgroups split each tile's columns with no exchange; two warps
+// per SM sub-partition hide each other's latencies on the chain
+// S^T -> P^T -> dV -> S^T of the next tile.  The warpgroups rebalance
+// registers (setmaxnreg): launched at 128 each, the last warpgroup gives
+// 64 up, the softmax warpgroups take 144 and the dQ warpgroup 160.
 // TMEM columns: S^T / P^T [0,128) dP^T / dQ [128,256) dK [256,256+D) dV [384,384+D).
 #include <cuda_bf16.h>
 
 #include "bda_internal.h"
 #include "bda_kernels.h"
+// The dK/dV kernel's warpgroups run under different register budgets.
+#define BDA_INLINE_SLOW_WAITS 1
 #include "bda_ptx.cuh"
 
 namespace bda {
@@ -108,7 +119,12 @@ __global__ void __launch_bounds__(256) bda_dq_convert_kernel(const float* __rest
 }
 
 // ------------------------------------------------------------------ dK/dV
-constexpr int kBwdThreads = 352;
+constexpr int kBwdThreads = 512;
+// Per-thread registers after the rebalancing (multiples of 8); per SM
+// sub-partition one warp of each warpgroup: 144 + 144 + 160 + 64 = 512
+// registers x 32 lanes = the launch's 128 x 4 warps.
+constexpr int kRegsSoftmax = 144, kRegsDq = 160, kRegsOther = 64, kRegsLaunch = 128;
+static_assert(2 * kRegsSoftmax + kRegsDq + kRegsOther == 4 * kRegsLaunch, "register split");
 constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
 constexpr uint32_t kDqBarrier = 1;  // named barrier of the dQ warpgroup (warps 4..7)
 constexpr uint32_t kMmaGate = 2;    // named barrier between the MMA warp and its waiter
@@ -205,17 +221,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(bar(L::B_DOFULL), 1);
     mbar_init(bar(L::B_SFULL), 1);
-    mbar_init(bar(L::B_PFULL), 128);
+    mbar_init(bar(L::B_PFULL), 256);
     mbar_init(bar(L::B_DVDONE), 1);
     mbar_init(bar(L::B_DPFULL), 1);
-    mbar_init(bar(L::B_DSFULL), 128);
+    mbar_init(bar(L::B_DSFULL), 256);
     mbar_init(bar(L::B_DQFULL), 1);
     mbar_init(bar(L::B_DQFREE), 128);
     mbar_init(bar(L::B_DSCONS), 1);
     mbar_init(bar(L::B_ACC), 1);
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -223,6 +239,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // Register rebalancing: every role starts by setting its warpgroup's
+  // budget (the decrease of warps 12..15 frees what the increases take; the
+  // launch holds exactly kRegsLaunch per thread) and runs to the end of the
+  // kernel on its own, so no code is shared between budgets.
+  auto finish = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 13) {
+      tc_fence_after();
+      tmem_dealloc(tbase, 512);
+    }
+  };
   // Failure-detection testing: CTA 0 leaves its first Q tile un-issued and
   // unannounced and waits only fault_timeout_ns for it (a.fault is 0 in
   // normal use).
@@ -244,201 +272,212 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto tile_h0 = [&](int i) -> int { return kvh * a.G + (i % n_sub) * a.hg; };
 
   bool ok = true;
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    int nq0 = 0, nq1 = 0, ndo = 0;  // copies issued per barrier (abort drain)
-    if (n_iter > 0) {
-      if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_do);
-        mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::TILE);
-        for (int c = 0; c < L::CH; ++c) {
-          tma_load_3d(base + L::K + c * L::CHUNK, &tm_k, bar(L::B_KV), c * 64, kvh, it.k_row);
-          tma_load_3d(base + L::V + c * L::CHUNK, &tm_v, bar(L::B_KV), c * 64, kvh, it.k_row);
-        }
-      }
-      // LSE and D of a query tile are fetched one tile ahead, into registers.
-      float lv[4], dv[4];
-      auto fetch = [&](int i) {
-        const int t0 = tile_t0(i), h0 = tile_h0(i);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int col = lane + 32 * k;
-          const int tok = t0 + (col >> a.lg_hg);
-          const int h = h0 + (col & (a.hg - 1));
-          lv[k] = INFINITY;
-          dv[k] = 0.f;
-          if (tok < it.lq) {
-            const size_t idx = size_t(h) * size_t(a.total_q) + size_t(it.q_row + tok);
-            lv[k] = a.lse[idx] * 1.4426950408889634f;
-            dv[k] = a.D[idx];
-          }
-        }
-      };
-      fetch(0);
-      for (int i = 0; i < n_iter; ++i) {
-        const int st = i & 1;
-        if (i >= 2 &&
-            !mbar_wait_warp(wc, bar(L::B_QEMPTY + st), uint32_t((i >> 1) - 1) & 1u)) {
-          ok = false;
-          break;
-        }
-        const int t0 = tile_t0(i), h0 = tile_h0(i);
-        const bool skip = fault_cta && i == 0;
-        if (lane == 0 && !skip) {
-          expect_tx(bar(L::B_QFULL + st), L::TILE);
-          for (int c = 0; c < L::CH; ++c)
-            tma_load_3d(base + L::Q + st * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + st),
-                        c * 64, h0, it.q_row + t0);
-        }
-        float* s_lse = reinterpret_cast<float*>(gbase + L::LSE) + 128 * st;
-        float* s_D = reinterpret_cast<float*>(gbase + L::DD) + 128 * st;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          s_lse[lane + 32 * k] = lv[k];
-          s_D[lane + 32 * k] = dv[k];
-        }
-        if (!skip) {
-          mbar_arrive(bar(L::B_QFULL + st));
-          if (st == 0) ++nq0; else ++nq1;
-        }
-        if (i + 1 < n_iter) fetch(i + 1);
-        // dO has one buffer: tile i's once dV of tile i-1 has read it
-        if (i >= 1 && !mbar_wait_warp(wc, bar(L::B_DVDONE), uint32_t(i - 1) & 1u)) {
-          ok = false;
-          break;
-        }
+  if (warp >= 12) {
+    // One decrease for the whole warpgroup (warps 12..15), then its roles.
+    setmaxnreg_dec<kRegsOther>();
+    if (warp == 12) {
+      // ------------------------------------------------------------ producer
+      int nq0 = 0, nq1 = 0, ndo = 0;  // copies issued per barrier (abort drain)
+      if (n_iter > 0) {
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(L::B_DOFULL), L::TILE);
-          for (int c = 0; c < L::CH; ++c)
-            tma_load_3d(base + L::DO + c * L::CHUNK, &tm_do, bar(L::B_DOFULL), c * 64, h0,
-                        it.q_row + t0);
-        }
-        ++ndo;
-      }
-      if ((!ok || *abort_flag) && lane == 0) {
-        drain_wait(wc, bar(L::B_KV), 0);
-        if (nq0) drain_wait(wc, bar(L::B_QFULL), uint32_t(nq0 - 1) & 1u);
-        if (nq1) drain_wait(wc, bar(L::B_QFULL + 1), uint32_t(nq1 - 1) & 1u);
-        if (ndo) drain_wait(wc, bar(L::B_DOFULL), uint32_t(ndo - 1) & 1u);
-      }
-    }
-  } else if (warp == 9 || warp == 10) {
-    // ----------------------------------------------------------------- MMA
-    // Warp 9 issues every MMA (lane 0); warp 10 waits on the mbarriers each
-    // product depends on and opens a named-barrier gate for it.  An mbarrier
-    // wait issued right behind a batch of MMAs queues behind them (hundreds
-    // of cycles even on a completed phase), while a named barrier costs a
-    // few cycles, so the issuing warp only ever meets named barriers.  The
-    // gate also carries the waiter's verdict: a failed wait stops both warps
-    // at the same gate.
-    const bool issuer = warp == 9;
-    auto gate = [&](bool wait_ok) -> bool { return named_bar_and(kMmaGate, 64, wait_ok); };
-    auto wt = [&](int b, uint32_t parity) -> bool { return mbar_wait_warp(wc, bar(b), parity); };
-    auto wt2 = [&](int b1, uint32_t p1, int b2, uint32_t p2) -> bool {
-      return mbar_wait2_warp(wc, bar(b1), p1, bar(b2), p2);
-    };
-    constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-    constexpr uint32_t idAcc = idesc_bf16(128, D, false, true);    // dV, dK
-    constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ
-    auto issue_s = [&](int i) {  // S_i^T = K Q_i^T
-      const uint32_t qa = base + L::Q + (i & 1) * L::TILE;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-        mma_ss(tbase + kColS, sdesc_sw128(base + L::K + off, 16, 1024),
-               sdesc_sw128(qa + off, 16, 1024), idSS, kk > 0);
-      }
-      mma_commit(bar(L::B_SFULL));
-    };
-    auto issue_dp = [&]() {  // dP^T = V dO^T
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-        mma_ss(tbase + kColDP, sdesc_sw128(base + L::V + off, 16, 1024),
-               sdesc_sw128(base + L::DO + off, 16, 1024), idSS, kk > 0);
-      }
-      mma_commit(bar(L::B_DPFULL));
-    };
-    if (n_iter > 0) {
-      bool go = gate(issuer || wt2(L::B_KV, 0, L::B_QFULL, 0));
-      if (go && issuer) {
-        tc_fence_after();
-        if (lane == 0) issue_s(0);
-      }
-      go = go && gate(issuer || wt(L::B_DOFULL, 0));
-      if (go && issuer) {
-        tc_fence_after();
-        if (lane == 0) issue_dp();
-      }
-      for (int i = 0; go && i < n_iter; ++i) {
-        const uint32_t ph = uint32_t(i) & 1u;
-        const int st = i & 1;
-        // dV += P^T dO, P^T (bf16 pairs) in the S^T columns
-        if (!(go = gate(issuer || wt(L::B_PFULL, ph)))) break;
-        if (issuer) {
-          tc_fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int kk = 0; kk < kTileM / 16; ++kk)
-              mma_ts(tbase + kColDV, tbase + kColS + 8u * kk,
-                     sdesc_sw128(base + L::DO + 2048u * kk, L::CHUNK, 1024), idAcc,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(bar(L::B_DVDONE));
+          tma_prefetch_desc(&tm_q);
+          tma_prefetch_desc(&tm_k);
+          tma_prefetch_desc(&tm_v);
+          tma_prefetch_desc(&tm_do);
+          mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::TILE);
+          for (int c = 0; c < L::CH; ++c) {
+            tma_load_3d(base + L::K + c * L::CHUNK, &tm_k, bar(L::B_KV), c * 64, kvh, it.k_row);
+            tma_load_3d(base + L::V + c * L::CHUNK, &tm_v, bar(L::B_KV), c * 64, kvh, it.k_row);
           }
         }
-        // next S^T once its Q is in and dV has read P^T out of the S^T columns
-        if (i + 1 < n_iter) {
-          if (!(go = gate(issuer || wt2(L::B_QFULL + (st ^ 1), uint32_t((i + 1) >> 1) & 1u,
-                                        L::B_DVDONE, ph))))
-            break;
-          if (issuer) {
-            tc_fence_after();
-            if (lane == 0) issue_s(i + 1);
-          }
-        }
-        // dQ = dS K, then dK += dS^T Q
-        if (!(go = gate(issuer || wt(L::B_DSFULL, ph)))) break;
-        if (issuer) {
-          tc_fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk)
-              mma_ss(tbase + kColDP, sdesc_sw128(base + L::DS + 2048u * kk, L::CHUNK, 1024),
-                     sdesc_sw128(base + L::K + 2048u * kk, L::CHUNK, 1024), idDQ, kk > 0);
-            mma_commit(bar(L::B_DQFULL));
-#pragma unroll
-            for (int kk = 0; kk < kTileM / 16; ++kk) {
-              const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-              mma_ss(tbase + kColDK, sdesc_sw128(base + L::DS + aoff, 16, 1024),
-                     sdesc_sw128(base + L::Q + st * L::TILE + 2048u * kk, L::CHUNK, 1024), idAcc,
-                     (i > 0 || kk > 0) ? 1u : 0u);
+        // LSE and D of a query tile are fetched one tile ahead, into registers.
+        float lv[4], dv[4];
+        auto fetch = [&](int i) {
+          const int t0 = tile_t0(i), h0 = tile_h0(i);
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int col = lane + 32 * k;
+            const int tok = t0 + (col >> a.lg_hg);
+            const int h = h0 + (col & (a.hg - 1));
+            lv[k] = INFINITY;
+            dv[k] = 0.f;
+            if (tok < it.lq) {
+              const size_t idx = size_t(h) * size_t(a.total_q) + size_t(it.q_row + tok);
+              lv[k] = a.lse[idx] * 1.4426950408889634f;
+              dv[k] = a.D[idx];
             }
-            mma_commit(bar(L::B_DSCONS));
-            mma_commit(bar(L::B_QEMPTY + st));
           }
-        }
-        // next dP^T once dQ has left the dP^T columns and dO_{i+1} is in
-        if (i + 1 < n_iter) {
-          if (!(go = gate(issuer || wt2(L::B_DOFULL, uint32_t(i + 1) & 1u, L::B_DQFREE, ph))))
+        };
+        fetch(0);
+        for (int i = 0; i < n_iter; ++i) {
+          const int st = i & 1;
+          if (i >= 2 &&
+              !mbar_wait_warp(wc, bar(L::B_QEMPTY + st), uint32_t((i >> 1) - 1) & 1u)) {
+            ok = false;
             break;
+          }
+          const int t0 = tile_t0(i), h0 = tile_h0(i);
+          const bool skip = fault_cta && i == 0;
+          if (lane == 0 && !skip) {
+            expect_tx(bar(L::B_QFULL + st), L::TILE);
+            for (int c = 0; c < L::CH; ++c)
+              tma_load_3d(base + L::Q + st * L::TILE + c * L::CHUNK, &tm_q, bar(L::B_QFULL + st),
+                          c * 64, h0, it.q_row + t0);
+          }
+          float* s_lse = reinterpret_cast<float*>(gbase + L::LSE) + 128 * st;
+          float* s_D = reinterpret_cast<float*>(gbase + L::DD) + 128 * st;
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            s_lse[lane + 32 * k] = lv[k];
+            s_D[lane + 32 * k] = dv[k];
+          }
+          if (!skip) {
+            mbar_arrive(bar(L::B_QFULL + st));
+            if (st == 0) ++nq0; else ++nq1;
+          }
+          if (i + 1 < n_iter) fetch(i + 1);
+          // dO has one buffer: tile i's once dV of tile i-1 has read it
+          if (i >= 1 && !mbar_wait_warp(wc, bar(L::B_DVDONE), uint32_t(i - 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(L::B_DOFULL), L::TILE);
+            for (int c = 0; c < L::CH; ++c)
+              tma_load_3d(base + L::DO + c * L::CHUNK, &tm_do, bar(L::B_DOFULL), c * 64, h0,
+                          it.q_row + t0);
+          }
+          ++ndo;
+        }
+        if ((!ok || *abort_flag) && lane == 0) {
+          drain_wait(wc, bar(L::B_KV), 0);
+          if (nq0) drain_wait(wc, bar(L::B_QFULL), uint32_t(nq0 - 1) & 1u);
+          if (nq1) drain_wait(wc, bar(L::B_QFULL + 1), uint32_t(nq1 - 1) & 1u);
+          if (ndo) drain_wait(wc, bar(L::B_DOFULL), uint32_t(ndo - 1) & 1u);
+        }
+      }
+    } else if (warp == 13 || warp == 14) {
+      // ----------------------------------------------------------------- MMA
+      // Warp 9 issues every MMA (lane 0); warp 10 waits on the mbarriers each
+      // product depends on and opens a named-barrier gate for it.  An mbarrier
+      // wait issued right behind a batch of MMAs queues behind them (hundreds
+      // of cycles even on a completed phase), while a named barrier costs a
+      // few cycles, so the issuing warp only ever meets named barriers.  The
+      // gate also carries the waiter's verdict: a failed wait stops both warps
+      // at the same gate.
+      const bool issuer = warp == 13;
+      auto gate = [&](bool wait_ok) -> bool { return named_bar_and(kMmaGate, 64, wait_ok); };
+      auto wt = [&](int b, uint32_t parity) -> bool { return mbar_wait_warp(wc, bar(b), parity); };
+      auto wt2 = [&](int b1, uint32_t p1, int b2, uint32_t p2) -> bool {
+        return mbar_wait2_warp(wc, bar(b1), p1, bar(b2), p2);
+      };
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t idAcc = idesc_bf16(128, D, false, true);    // dV, dK
+      constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ
+      auto issue_s = [&](int i) {  // S_i^T = K Q_i^T
+        const uint32_t qa = base + L::Q + (i & 1) * L::TILE;
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+          mma_ss(tbase + kColS, sdesc_sw128(base + L::K + off, 16, 1024),
+                 sdesc_sw128(qa + off, 16, 1024), idSS, kk > 0);
+        }
+        mma_commit(bar(L::B_SFULL));
+      };
+      auto issue_dp = [&]() {  // dP^T = V dO^T
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+          mma_ss(tbase + kColDP, sdesc_sw128(base + L::V + off, 16, 1024),
+                 sdesc_sw128(base + L::DO + off, 16, 1024), idSS, kk > 0);
+        }
+        mma_commit(bar(L::B_DPFULL));
+      };
+      if (n_iter > 0) {
+        bool go = gate(issuer || wt2(L::B_KV, 0, L::B_QFULL, 0));
+        if (go && issuer) {
+          tc_fence_after();
+          if (lane == 0) issue_s(0);
+        }
+        go = go && gate(issuer || wt(L::B_DOFULL, 0));
+        if (go && issuer) {
+          tc_fence_after();
+          if (lane == 0) issue_dp();
+        }
+        for (int i = 0; go && i < n_iter; ++i) {
+          const uint32_t ph = uint32_t(i) & 1u;
+          const int st = i & 1;
+          // dV += P^T dO, P^T (bf16 pairs) in the S^T columns
+          if (!(go = gate(issuer || wt(L::B_PFULL, ph)))) break;
           if (issuer) {
             tc_fence_after();
-            if (lane == 0) issue_dp();
+            if (lane == 0) {
+  #pragma unroll
+              for (int kk = 0; kk < kTileM / 16; ++kk)
+                // P^T of query columns [0,64) sits in TMEM columns [0,32), of
+                // [64,128) in [64,96) (each softmax warpgroup writes its half
+                // over its own S^T columns)
+                mma_ts(tbase + kColDV, tbase + kColS + 8u * kk + (kk >= 4 ? 32u : 0u),
+                       sdesc_sw128(base + L::DO + 2048u * kk, L::CHUNK, 1024), idAcc,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(bar(L::B_DVDONE));
+            }
+          }
+          // next S^T once its Q is in and dV has read P^T out of the S^T columns
+          if (i + 1 < n_iter) {
+            if (!(go = gate(issuer || wt2(L::B_QFULL + (st ^ 1), uint32_t((i + 1) >> 1) & 1u,
+                                          L::B_DVDONE, ph))))
+              break;
+            if (issuer) {
+              tc_fence_after();
+              if (lane == 0) issue_s(i + 1);
+            }
+          }
+          // dQ = dS K, then dK += dS^T Q
+          if (!(go = gate(issuer || wt(L::B_DSFULL, ph)))) break;
+          if (issuer) {
+            tc_fence_after();
+            if (lane == 0) {
+  #pragma unroll
+              for (int kk = 0; kk < kTileN / 16; ++kk)
+                mma_ss(tbase + kColDP, sdesc_sw128(base + L::DS + 2048u * kk, L::CHUNK, 1024),
+                       sdesc_sw128(base + L::K + 2048u * kk, L::CHUNK, 1024), idDQ, kk > 0);
+              mma_commit(bar(L::B_DQFULL));
+  #pragma unroll
+              for (int kk = 0; kk < kTileM / 16; ++kk) {
+                const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
+                mma_ss(tbase + kColDK, sdesc_sw128(base + L::DS + aoff, 16, 1024),
+                       sdesc_sw128(base + L::Q + st * L::TILE + 2048u * kk, L::CHUNK, 1024), idAcc,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(bar(L::B_DSCONS));
+              mma_commit(bar(L::B_QEMPTY + st));
+            }
+          }
+          // next dP^T once dQ has left the dP^T columns and dO_{i+1} is in
+          if (i + 1 < n_iter) {
+            if (!(go = gate(issuer || wt2(L::B_DOFULL, uint32_t(i + 1) & 1u, L::B_DQFREE, ph))))
+              break;
+            if (issuer) {
+              tc_fence_after();
+              if (lane == 0) issue_dp();
+            }
           }
         }
+        ok = go;
+        if (issuer && lane == 0) {
+          mma_commit(bar(L::B_ACC));
+          drain_wait(wc, bar(L::B_ACC), 0);
+        }
       }
-      ok = go;
-      if (issuer && lane == 0) {
-        mma_commit(bar(L::B_ACC));
-        drain_wait(wc, bar(L::B_ACC), 0);
-      }
-    }
-  } else if (warp < 4) {
+    }  // warp 15: idle
+    finish();
+  } else if (warp < 8) {
     // ------------------------------------------------------------- softmax
-    const int kr = tid;  // TMEM lane == key row of the tile
+    setmaxnreg_inc<kRegsSoftmax>();
+    const int kr = tid & 127;  // TMEM lane == key row of the tile
+    const int half = warp >> 2;  // query columns [64 half, 64 half + 64)
+    const int c0 = 2 * half;     // its 32-column chunks c0, c0 + 1
     const bool key_valid = kr < it.k_len;
     // Query positions that see this key: [lo, hi) and [lo2, hi2).
     const KeyRows kq = MULTI ? key_rows(it.kpos0 + kr, it.prefix, a.block, it.lk,
@@ -446,7 +485,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                              : key_rows(it.kpos0 + kr, it.prefix, a.block, it.lk);
     const int q_hi = min(kq.hi - delta, it.lq);  // local query tokens [kq.lo - delta, q_hi)
     const int q2_lo = kq.lo2 - delta, q2_hi = min(kq.hi2 - delta, it.lq);
-    const uint32_t lane_addr = tbase + (uint32_t(warp * 32) << 16);
+    const uint32_t lane_addr = tbase + (uint32_t((warp & 3) * 32) << 16);
     const float sl2 = a.scale_log2;
     uint8_t* dsb = gbase + L::DS;
     for (int i = 0; i < n_iter; ++i) {
@@ -468,8 +507,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         c_lo2 = max(lo2_c, 0) << a.lg_hg;
         c_hi2 = hi2_c <= lo2_c ? c_lo2 : min(hi2_c, a.tok) << a.lg_hg;
       }
-      const bool warp_full = __all_sync(0xffffffffu, (c_lo == 0 && c_hi >= kTileM) ||
-                                                         (MULTI && c_lo2 == 0 && c_hi2 >= kTileM));
+      // Warps whose rows all see this warpgroup's 64 columns skip masking.
+      const int h_lo = 64 * half, h_hi = h_lo + 64;
+      const bool warp_full = __all_sync(0xffffffffu, (c_lo <= h_lo && c_hi >= h_hi) ||
+                                                         (MULTI && c_lo2 <= h_lo && c_hi2 >= h_hi));
       // QFULL publishes the producer's LSE / D staging to these threads.
       if (!mbar_wait2_warp(wc, bar(L::B_QFULL + st), uint32_t(i >> 1) & 1u, bar(L::B_SFULL), ph)) {
         ok = false;
@@ -477,9 +518,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_after();
       // P^T = exp(scale S^T - LSE), masked, 32 query columns at a time; the
-      // bf16 pairs go back into the S^T columns already read (chunk c fills
-      // columns [16c, 16c+16)) for the dV MMA, and stay in registers for dS.
-      uint32_t pp[kTileM / 2];
+      // bf16 pairs go back into this warpgroup's S^T columns already read
+      // (chunk c fills columns [16c + 32 half, +16)) for the dV MMA, and stay
+      // in registers for dS.
+      uint32_t pp[kTileM / 4];
       auto p_chunk = [&](int c, const uint32_t (&r)[32]) {
         uint32_t pk[16];
 #pragma unroll
@@ -506,23 +548,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) pp[16 * c + j] = pk[j];
-        tmem_st16(lane_addr + kColS + 16u * c, pk);
+        for (int j = 0; j < 16; ++j) pp[16 * (c - c0) + j] = pk[j];
+        tmem_st16(lane_addr + kColS + 16u * uint32_t(c) + 32u * uint32_t(half), pk);
       };
       {
         uint32_t ra[32], rb[32];
-        tmem_ld32(lane_addr + kColS, ra);
+        tmem_ld32(lane_addr + kColS + 32u * uint32_t(c0), ra);
+        tmem_ld32(lane_addr + kColS + 32u * uint32_t(c0 + 1), rb);
         tmem_ld_wait(ra);
-        tmem_ld32(lane_addr + kColS + 32u, rb);
-        p_chunk(0, ra);
+        p_chunk(c0, ra);
         tmem_ld_wait(rb);
-        tmem_ld32(lane_addr + kColS + 64u, ra);
-        p_chunk(1, rb);
-        tmem_ld_wait(ra);
-        tmem_ld32(lane_addr + kColS + 96u, rb);
-        p_chunk(2, ra);
-        tmem_ld_wait(rb);
-        p_chunk(3, rb);
+        p_chunk(c0 + 1, rb);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -545,7 +581,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // dP - D in fp32, rounded to a bf16 pair, times the bf16 pair of
             // P in one packed multiply (dS is stored as bf16 anyway).
             const int cc = 8 * u4 + 2 * j;
-            pk[j] = mul_bf16x2(pp[16 * c + 4 * u4 + j],
+            pk[j] = mul_bf16x2(pp[16 * (c - c0) + 4 * u4 + j],
                                pack_bf16x2(__uint_as_float(r[cc]) - dd[2 * j],
                                            __uint_as_float(r[cc + 1]) - dd[2 * j + 1]));
           }
@@ -556,28 +592,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       {
         uint32_t ra[32], rb[32];
-        tmem_ld32(lane_addr + kColDP, ra);
+        tmem_ld32(lane_addr + kColDP + 32u * uint32_t(c0), ra);
+        tmem_ld32(lane_addr + kColDP + 32u * uint32_t(c0 + 1), rb);
         tmem_ld_wait(ra);
-        tmem_ld32(lane_addr + kColDP + 32u, rb);
-        ds_chunk(0, ra);
+        ds_chunk(c0, ra);
         tmem_ld_wait(rb);
-        tmem_ld32(lane_addr + kColDP + 64u, ra);
-        ds_chunk(1, rb);
-        tmem_ld_wait(ra);
-        tmem_ld32(lane_addr + kColDP + 96u, rb);
-        ds_chunk(2, ra);
-        tmem_ld_wait(rb);
-        ds_chunk(3, rb);
+        ds_chunk(c0 + 1, rb);
       }
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar(L::B_DSFULL));
     }
-  } else {
+    // ------------------------------------------- dK (warps 0-3), dV (4-7)
+    {
+    const int row = tid & 127;
+    const bool is_dk = warp < 4;
+    const uint32_t lane_addr = tbase + (uint32_t((warp & 3) * 32) << 16);
+    const bool have = n_iter > 0 && ok && !*abort_flag;
+    bool acc_ok = false;
+    if (have) acc_ok = mbar_wait_warp(wc, bar(L::B_ACC), 0);
+    if (have && acc_ok) tc_fence_after();
+    if (n_iter == 0 || acc_ok) {
+      __nv_bfloat16* dst = (is_dk ? a.dk : a.dv) +
+                           (size_t(it.k_row + row) * size_t(a.hkv) + size_t(kvh)) * size_t(D);
+      const float mul = is_dk ? a.scale : 1.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        if (n_iter > 0) {
+          tmem_ld32(lane_addr + (is_dk ? kColDK : kColDV) + 32u * c, rr);
+          tmem_ld_wait(rr);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rr[j] = 0u;
+        }
+        if (row < it.k_len) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(__uint_as_float(rr[2 * j]) * mul, __uint_as_float(rr[2 * j + 1]) * mul);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+    }
+    }
+    finish();
+  } else if (warp < 12) {
     // ------------------------------------------- dQ: TMEM -> smem -> TMA add
-    const int qc = tid - 128;  // TMEM lane == query row of the tile
+    setmaxnreg_inc<kRegsDq>();
+    const int qc = tid - 256;  // TMEM lane == query row of the tile
     const bool leader = qc == 0;
-    const uint32_t lane_addr = tbase + (uint32_t((warp - 4) * 32) << 16);
+    const uint32_t lane_addr = tbase + (uint32_t((warp - 8) * 32) << 16);
     uint32_t n_chunks = 0;  // staging buffers handed to the TMA so far
     for (int i = 0; i < n_iter; ++i) {
       // All four warps leave together, so none is left at a named barrier.
@@ -615,50 +682,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     if (leader) bulk_wait_all();
+    finish();
   }
 
-  // ----------------------------------------------- dK (warps 0-3), dV (4-7)
-  if (warp < 8) {
-    const int row = tid & 127;
-    const bool is_dk = warp < 4;
-    const uint32_t lane_addr = tbase + (uint32_t((warp & 3) * 32) << 16);
-    const bool have = n_iter > 0 && ok && !*abort_flag;
-    bool acc_ok = false;
-    if (have) acc_ok = mbar_wait_warp(wc, bar(L::B_ACC), 0);
-    if (have && acc_ok) tc_fence_after();
-    if (n_iter == 0 || acc_ok) {
-      __nv_bfloat16* dst = (is_dk ? a.dk : a.dv) +
-                           (size_t(it.k_row + row) * size_t(a.hkv) + size_t(kvh)) * size_t(D);
-      const float mul = is_dk ? a.scale : 1.f;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        if (n_iter > 0) {
-          tmem_ld32(lane_addr + (is_dk ? kColDK : kColDV) + 32u * c, rr);
-          tmem_ld_wait(rr);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) rr[j] = 0u;
-        }
-        if (row < it.k_len) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(__uint_as_float(rr[2 * j]) * mul, __uint_as_float(rr[2 * j + 1]) * mul);
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 512);
-  }
 }
 
 template <int D, bool MULTI>
@@ -666,9 +692,20 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
                           int n_items, cudaStream_t stream) {
   using L = BwdLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(bda_bwd_dkdv_kernel<D, MULTI>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::BYTES));
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = once_per_device(smem_set, [] {
+    return cudaFuncSetAttribute(bda_bwd_dkdv_kernel<D, MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(L::BYTES));
+  });
   if (e != cudaSuccess) return e;
+  // The warpgroups' register increases take exactly what the decrease frees
+  // from a launch of kRegsLaunch per thread; any other allocation would leave
+  // an increase waiting, so refuse to launch then.
+  static const int regs = [] {
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, bda_bwd_dkdv_kernel<D, MULTI>) == cudaSuccess ? fa.numRegs : -1;
+  }();
+  if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const unsigned grid = unsigned(n_items) * unsigned(a.hkv);
   bda_bwd_dkdv_kernel<D, MULTI><<<grid, kBwdThreads, L::BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();

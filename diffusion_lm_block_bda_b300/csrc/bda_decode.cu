@@ -445,14 +445,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         a.lse[size_t(head0 + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
             lse2 * 0.69314718055994530942f;
       } else if (row_valid) {
-        // Partial of this chunk: normalised O (fp32, row-fastest so a warp's
-        // stores and the combine's loads are contiguous) and its log2 LSE.
+        // Partial of this chunk: normalised O and its log2 LSE.  O is laid
+        // out [D/4][128 rows][4] per slot, so a warp's float4 stores (and the
+        // combine's float4 loads) cover 32 consecutive rows contiguously.
         const size_t slot = size_t(dj.part) * size_t(a.n_groups) + size_t(grp);
-        float* po = a.part_o + slot * size_t(D) * kTileM + r;
+        float4* po = reinterpret_cast<float4*>(a.part_o) + slot * size_t(D / 4) * kTileM + r;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) po[size_t(32 * c + i) * kTileM] = __uint_as_float(ov[c][i]) * inv_l;
+          for (int i = 0; i < 8; ++i)
+            po[size_t(8 * c + i) * kTileM] = make_float4(
+                __uint_as_float(ov[c][4 * i]) * inv_l, __uint_as_float(ov[c][4 * i + 1]) * inv_l,
+                __uint_as_float(ov[c][4 * i + 2]) * inv_l, __uint_as_float(ov[c][4 * i + 3]) * inv_l);
         a.part_lse[slot * kTileM + r] = lse2;
       }
     }
@@ -467,43 +471,57 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 }
 
 // Merges the chunks of every split query tile.  Block = (forward item, head
-// group, 16 of the D columns); thread r = tile row r, so for each chunk and
-// column a warp's loads are 32 consecutive floats.
+// group, 4 of the D columns); thread r = tile row r, so for each chunk a
+// warp's float4 loads cover 32 consecutive rows.  The chunk loop is unrolled
+// so several chunks' loads are in flight at once (the partials sit in L2).
 template <int D>
 __global__ void __launch_bounds__(kTileM) bda_fwd_combine_kernel(const FwdArgs a) {
   // Wait for the split kernel (this grid may have launched while it ran).
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  constexpr int NSL = D / 16;
+  constexpr int NQ = D / 4;
   const int b = blockIdx.x;
-  const int sl = b % NSL, rest = b / NSL;
+  const int q = b % NQ, rest = b / NQ;
   const int grp = rest % a.n_groups, item = rest / a.n_groups;
   const FwdItem it = a.items[item];
   if (it.n_split <= 1) return;
   const int r = threadIdx.x, t_local = r >> a.lg_hg, hh = r & (a.hg - 1);
   if (t_local >= it.q_len) return;
-  auto slot = [&](int s) -> size_t { return size_t(it.part0 + s) * size_t(a.n_groups) + size_t(grp); };
-  float M = -INFINITY;
-  for (int s = 0; s < it.n_split; ++s) M = fmaxf(M, a.part_lse[slot(s) * kTileM + r]);
-  float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  float Lsum = 0.f;
+  const size_t slot0 = size_t(it.part0) * size_t(a.n_groups) + size_t(grp);
+  const size_t sstride = size_t(a.n_groups);  // slots of consecutive chunks
+  const float* pl = a.part_lse + slot0 * kTileM + r;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o) + (slot0 * NQ + size_t(q)) * kTileM + r;
+  // One pass over the chunks with a running maximum (as in an online
+  // softmax): a chunk whose LSE exceeds the maximum so far rescales the sums.
+  float M = -INFINITY, Lsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
   for (int s = 0; s < it.n_split; ++s) {
-    const float w = ex2(a.part_lse[slot(s) * kTileM + r] - M);
+    const float ls = pl[size_t(s) * sstride * kTileM];
+    const float4 v = po[size_t(s) * sstride * NQ * kTileM];
+    if (ls > M) {
+      const float c = ex2(M - ls);  // 0 while M is -inf
+      Lsum *= c;
+      acc.x *= c;
+      acc.y *= c;
+      acc.z *= c;
+      acc.w *= c;
+      M = ls;
+    }
+    // 0 for a chunk that saw none of this row's keys (its LSE is -inf, and M
+    // may still be -inf, where ls - M would be NaN)
+    const float w = ls > -INFINITY ? ex2(ls - M) : 0.f;
     Lsum += w;
-    const float* ps = a.part_o + (slot(s) * size_t(D) + size_t(16 * sl)) * kTileM + r;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = fmaf(w, ps[size_t(i) * kTileM], acc[i]);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
   }
   const float inv = 1.f / Lsum;
-  uint32_t pk[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
   __nv_bfloat16* orow =
-      a.o + (size_t(it.q_row + t_local) * a.hq + size_t(grp * a.hg + hh)) * size_t(D) + 16 * sl;
-  reinterpret_cast<uint4*>(orow)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  reinterpret_cast<uint4*>(orow)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-  if (sl == 0)
+      a.o + (size_t(it.q_row + t_local) * a.hq + size_t(grp * a.hg + hh)) * size_t(D) + 4 * q;
+  *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
+                                               pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (q == 0)
     a.lse[size_t(grp * a.hg + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
         (M + log2f(Lsum)) * 0.69314718055994530942f;
 }
@@ -514,14 +532,17 @@ cudaError_t launch_decode_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             cudaStream_t stream) {
   using L = DecLayout<D, KV8>;
   static_assert(L::ALLOC <= 232448, "decode shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(bda_decode_kernel<D, KV8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::ALLOC));
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = once_per_device(smem_set, [] {
+    return cudaFuncSetAttribute(bda_decode_kernel<D, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(L::ALLOC));
+  });
   if (e != cudaSuccess) return e;
   const unsigned grid = unsigned(n_dec) * unsigned(a.n_groups);
   bda_decode_kernel<D, KV8><<<grid, kDecThreads, L::ALLOC, stream>>>(tq, tk, tv, a);
   if ((e = cudaGetLastError()) != cudaSuccess || !combine) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(n_items) * unsigned(a.n_groups) * unsigned(D / 16));
+  cfg.gridDim = dim3(unsigned(n_items) * unsigned(a.n_groups) * unsigned(D / 4));
   cfg.blockDim = dim3(kTileM);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

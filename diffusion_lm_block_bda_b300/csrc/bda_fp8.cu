@@ -47,10 +47,14 @@ __global__ void __launch_bounds__(32) bda_fp8_scales_init_kernel(float* scale, i
 }
 
 // max |x| per head into scale[] (as the bits of a non-negative float, whose
-// integer order is the float order).
+// integer order is the float order): each block reduces into shared memory,
+// then adds one global atomic per head it saw.
 __global__ void __launch_bounds__(256) bda_fp8_absmax_kernel(const uint4* __restrict__ x,
                                                              float* __restrict__ scale, int64_t n8,
                                                              int heads, int d8) {
+  extern __shared__ unsigned int blk_max[];
+  for (int h = threadIdx.x; h < heads; h += blockDim.x) blk_max[h] = 0u;
+  __syncthreads();
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
     const uint4 v = x[i];
@@ -61,10 +65,12 @@ __global__ void __launch_bounds__(256) bda_fp8_absmax_kernel(const uint4* __rest
       m = max(m, (w[k] << 16) & 0x7fffffffu);
       m = max(m, w[k] & 0x7fff0000u);
     }
-    const int h = int((i / d8) % heads);
     // NaN bits sort above every finite value; a NaN input yields a NaN scale
-    if (m) atomicMax(reinterpret_cast<unsigned int*>(scale) + h, m);
+    if (m) atomicMax(blk_max + int((i / d8) % heads), m);
   }
+  __syncthreads();
+  for (int h = threadIdx.x; h < heads; h += blockDim.x)
+    if (blk_max[h]) atomicMax(reinterpret_cast<unsigned int*>(scale) + h, blk_max[h]);
 }
 
 __global__ void __launch_bounds__(32) bda_fp8_scales_final_kernel(float* scale, int heads) {
@@ -109,8 +115,8 @@ cudaError_t launch_fp8_scales(const __nv_bfloat16* x, float* scale, int64_t rows
   if (e != cudaSuccess) return e;
   const int64_t n8 = rows * heads * d / 8;
   if (n8 > 0) {
-    bda_fp8_absmax_kernel<<<grid_for(n8), 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), scale,
-                                                            n8, heads, d / 8);
+    bda_fp8_absmax_kernel<<<grid_for(n8), 256, sizeof(unsigned int) * size_t(heads), stream>>>(
+        reinterpret_cast<const uint4*>(x), scale, n8, heads, d / 8);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   bda_fp8_scales_final_kernel<<<1, 32, 0, stream>>>(scale, heads);

@@ -30,9 +30,12 @@ struct Shape {
 // A problem with fewer than kSplitMaxUnits forward units (query tile x head
 // group) fills under half of a B300's 148 SMs; its forward splits the key
 // tiles of each query tile into chunks of split_c tiles, split_c chosen so
-// the units number about kSplitTargetUnits.
+// the units number about kSplitTargetUnits.  Half the SMs with two key tiles
+// each beat one tile on every SM for the decode step (14.3 against 16.4 us):
+// each unit overlaps its second tile's loads with its first tile's work and
+// writes half as many partial results.
 constexpr int kSplitMaxUnits = 74;
-constexpr int kSplitTargetUnits = 148;
+constexpr int kSplitTargetUnits = 74;
 
 // Validates the problem and mask; fills `s`.  Host-only, launches nothing.
 // A multi-block staircase whose non-empty groups are not in block order
@@ -48,7 +51,7 @@ size_t plan_bytes(const Shape& s, bool with_bwd = true);
 size_t plan_group_offset(const Shape& s, bool with_bwd);
 size_t plan_dec_offset(const Shape& s, bool with_bwd);
 // Workspace: the plan, then the split forward's partial results (fp32 O
-// [n_parts * n_groups][d][128] and log2 LSE [n_parts * n_groups][128]).
+// [n_parts * n_groups][d/4][128][4] and log2 LSE [n_parts * n_groups][128]).
 size_t ws_offset_parts(const Shape& s);
 size_t ws_offset_part_lse(const Shape& s);
 size_t workspace_bytes(const Shape& s, bool with_bwd);

@@ -1,6 +1,7 @@
 // bda_kernels.h -- launchers of the CUDA kernels (internal; the public surface
 // is include/bda_attn.h).
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -10,6 +11,21 @@
 #include "bda_internal.h"
 
 namespace bda {
+
+// Runs `set` (a kernel attribute change) once per device for the call site
+// that owns `done`: attributes persist, and changing one before every launch
+// costs host time on each call.
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, F set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  if ((e = set()) != cudaSuccess) return e;
+  done.fetch_or(bit, std::memory_order_release);
+  return cudaSuccess;
+}
 
 struct FwdArgs {
   const FwdItem* items;
@@ -36,7 +52,7 @@ struct FwdArgs {
   // Split (decode) forward: its units, and the workspace's partial results
   // (null when the plan splits no item).
   const DecItem* dec;
-  float* part_o;    // [n_parts * n_groups][D][128] fp32, normalised O of a chunk
+  float* part_o;    // [n_parts * n_groups][D/4][128][4] fp32, normalised O of a chunk
   float* part_lse;  // [n_parts * n_groups][128] fp32, log2 LSE of a chunk
   // FP8 K/V: per-KV-head dequantisation scales (device, fp32 [hkv]).
   const float* k_scale;

@@ -70,7 +70,14 @@ __device__ __forceinline__ void raise_abort(WaitCtx w, uint32_t code) {
 // does not succeed at once enters the out-of-line loop (a call at every site
 // measured slower in the kernels, and a fully inlined loop slower still in
 // the backward, whose many wait sites it bloats).
+// A kernel whose warpgroups run under different register budgets
+// (setmaxnreg) cannot call a shared out-of-line function; such a translation
+// unit defines BDA_INLINE_SLOW_WAITS before including this header.
+#ifdef BDA_INLINE_SLOW_WAITS
+static __device__ __forceinline__ bool mbar_wait_slow(WaitCtx w, uint32_t bar, uint32_t parity) {
+#else
 static __device__ __noinline__ bool mbar_wait_slow(WaitCtx w, uint32_t bar, uint32_t parity) {
+#endif
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -176,6 +183,19 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
       : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
       : "memory");
   return r != 0;
+}
+
+// ------------------------------------------------- register rebalancing
+// Warpgroup-wide change of the per-thread register budget (every warp of
+// the warpgroup executes it); an increase waits until decreases elsewhere in
+// the CTA have freed the registers.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------- tcgen05

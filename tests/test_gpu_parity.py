@@ -34,9 +34,9 @@ def test_tiny_block_causal_c1():
 
 
 def test_decode_step_c2():
-    """The decode step takes the split forward (17 key tiles x 8 head groups
-    as 136 CTAs, merged by the combine kernel); the persistent forward must
-    agree with the oracle too."""
+    """The decode step takes the split forward (its 17 key tiles as 9 chunks
+    x 8 head groups = 72 CTAs, merged by the combine kernel); the persistent
+    forward must agree with the oracle too."""
     import diffusion_lm_block_bda_b300 as bda
     from diffusion_lm_block_bda_b300 import Problem
     w = W.named("c2")
@@ -44,7 +44,7 @@ def test_decode_step_c2():
     buf = torch.zeros(bda.bda_attn_plan_size(pb), dtype=torch.uint8)
     bda.bda_attn_plan_host(pb, buf)
     hdr = buf[:64].numpy().view(np.int32)
-    assert hdr[11] == 1 and hdr[9] == 17 and hdr[10] == 17  # split_c, n_dec, n_parts
+    assert hdr[11] == 2 and hdr[9] == 9 and hdr[10] == 9  # split_c, n_dec, n_parts
     inp = W.make_inputs(w, seed=0)
     ref = oracle_full(w, inp, with_bwd=False)
     compare_full(w, inp, gpu_run(w, inp, with_bwd=False), with_bwd=False, ref=ref)

@@ -240,17 +240,17 @@ def test_planner_named_workloads(name):
 
 def test_split_forward_plans():
     """Problems with fewer than 74 query-tile units split their key tiles so
-    the units number about 148; larger ones are not split."""
+    the units number about 74; larger ones are not split."""
     def header(pb):
         buf = torch.zeros(bda.bda_attn_plan_size(pb), dtype=torch.uint8)
         bda.bda_attn_plan_host(pb, buf)
         h = buf[:64].numpy().view(np.int32)
         return int(h[9]), int(h[10]), int(h[11])  # n_dec, n_parts, split_c
     c2 = Problem.from_workload(W.named("c2"))
-    assert header(c2) == (17, 17, 1)  # 17 key tiles x 8 head groups = 136 units
+    assert header(c2) == (9, 9, 2)  # 17 key tiles x 8 head groups: 9 chunks of <= 2 tiles
     long_decode = Problem([0, 32], [0, 32 * 1024], 32, 8, 128, W.BLOCK_CAUSAL, 32)
-    n_dec, n_parts, c = header(long_decode)  # 256 tiles x 8 groups: chunks of 14
-    assert c == 14 and n_dec == n_parts == 19
+    n_dec, n_parts, c = header(long_decode)  # 256 tiles x 8 groups: chunks of 28
+    assert c == 28 and n_dec == n_parts == 10
     assert header(Problem.from_workload(W.named("c3")))[2] == 0
     check_plan(W.custom(W.BLOCK_CAUSAL, 32, 32, 8, 128, [32, 32, 5], [2080, 700, 133]))
 
