@@ -374,22 +374,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idAcc = idesc_bf16(128, D, false, true);    // dV, dK
       constexpr uint32_t idDQ = idesc_bf16(128, D, true, true);      // dQ
+      // Lean issue (one add per operand per MMA, literal accumulate flag):
+      // the issuing lane shares its sub-partition with a P/dS warp.
       auto issue_s = [&](int i) {  // S_i^T = K Q_i^T
-        const uint32_t qa = base + L::Q + (i & 1) * L::TILE;
+        const uint32_t kl = opaque(sdesc_lo(base + L::K, 16));
+        const uint32_t ql = opaque(sdesc_lo(base + L::Q + (i & 1) * L::TILE, 16));
+        mma_ss_c<false>(tbase + kColS, sdesc_of_lo(kl), sdesc_of_lo(ql), idSS);
   #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColS, sdesc_sw128(base + L::K + off, 16, 1024),
-                 sdesc_sw128(qa + off, 16, 1024), idSS, kk > 0);
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u) >> 4;
+          mma_ss_c<true>(tbase + kColS, sdesc_of_lo(kl + off), sdesc_of_lo(ql + off), idSS);
         }
         mma_commit(bar(L::B_SFULL));
       };
       auto issue_dp = [&]() {  // dP^T = V dO^T
+        const uint32_t vl = opaque(sdesc_lo(base + L::V, 16));
+        const uint32_t ol = opaque(sdesc_lo(base + L::DO, 16));
+        mma_ss_c<false>(tbase + kColDP, sdesc_of_lo(vl), sdesc_of_lo(ol), idSS);
   #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColDP, sdesc_sw128(base + L::V + off, 16, 1024),
-                 sdesc_sw128(base + L::DO + off, 16, 1024), idSS, kk > 0);
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u) >> 4;
+          mma_ss_c<true>(tbase + kColDP, sdesc_of_lo(vl + off), sdesc_of_lo(ol + off), idSS);
         }
         mma_commit(bar(L::B_DPFULL));
       };
@@ -412,14 +417,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (issuer) {
             tc_fence_after();
             if (lane == 0) {
+              const uint32_t ol = opaque(sdesc_lo(base + L::DO, L::CHUNK));
+              mma_ts(tbase + kColDV, tbase + kColS, sdesc_of_lo(ol), idAcc, i > 0 ? 1u : 0u);
   #pragma unroll
-              for (int kk = 0; kk < kTileM / 16; ++kk)
-                // P^T of query columns [0,64) sits in TMEM columns [0,32), of
-                // [64,128) in [64,96) (each softmax warpgroup writes its half
-                // over its own S^T columns)
-                mma_ts(tbase + kColDV, tbase + kColS + 8u * kk + (kk >= 4 ? 32u : 0u),
-                       sdesc_sw128(base + L::DO + 2048u * kk, L::CHUNK, 1024), idAcc,
-                       (i > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 1; kk < kTileM / 16; ++kk)
+                mma_ts_c<true>(tbase + kColDV, tbase + kColS + 8u * kk + (kk >= 4 ? 32u : 0u),
+                               sdesc_of_lo(ol + ((2048u * kk) >> 4)), idAcc);
               mma_commit(bar(L::B_DVDONE));
             }
           }
@@ -438,17 +441,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (issuer) {
             tc_fence_after();
             if (lane == 0) {
+              const uint32_t sl = opaque(sdesc_lo(base + L::DS, L::CHUNK));
+              const uint32_t kl = opaque(sdesc_lo(base + L::K, L::CHUNK));
+              mma_ss_c<false>(tbase + kColDP, sdesc_of_lo(sl), sdesc_of_lo(kl), idDQ);
   #pragma unroll
-              for (int kk = 0; kk < kTileN / 16; ++kk)
-                mma_ss(tbase + kColDP, sdesc_sw128(base + L::DS + 2048u * kk, L::CHUNK, 1024),
-                       sdesc_sw128(base + L::K + 2048u * kk, L::CHUNK, 1024), idDQ, kk > 0);
+              for (int kk = 1; kk < kTileN / 16; ++kk)
+                mma_ss_c<true>(tbase + kColDP, sdesc_of_lo(sl + ((2048u * kk) >> 4)),
+                               sdesc_of_lo(kl + ((2048u * kk) >> 4)), idDQ);
               mma_commit(bar(L::B_DQFULL));
+              const uint32_t tl = opaque(sdesc_lo(base + L::DS, 16));
+              const uint32_t ql = opaque(sdesc_lo(base + L::Q + st * L::TILE, L::CHUNK));
+              mma_ss(tbase + kColDK, sdesc_of_lo(tl), sdesc_of_lo(ql), idAcc, i > 0 ? 1u : 0u);
   #pragma unroll
-              for (int kk = 0; kk < kTileM / 16; ++kk) {
-                const uint32_t aoff = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-                mma_ss(tbase + kColDK, sdesc_sw128(base + L::DS + aoff, 16, 1024),
-                       sdesc_sw128(base + L::Q + st * L::TILE + 2048u * kk, L::CHUNK, 1024), idAcc,
-                       (i > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 1; kk < kTileM / 16; ++kk) {
+                const uint32_t aoff = (uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u) >> 4;
+                mma_ss_c<true>(tbase + kColDK, sdesc_of_lo(tl + aoff),
+                               sdesc_of_lo(ql + ((2048u * kk) >> 4)), idAcc);
               }
               mma_commit(bar(L::B_DSCONS));
               mma_commit(bar(L::B_QEMPTY + st));

@@ -251,23 +251,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
       auto issue_s = [&](int j) {
         const int s = j & 1;
-        const uint32_t ka = base + L::KB + s * L::TILE;
+        const uint32_t ql = opaque(sdesc_lo(base + L::Q, 16));
+        const uint32_t kl = opaque(sdesc_lo(base + L::KB + s * L::TILE, 16));
+        mma_ss_c<false>(tbase + kColS, sdesc_of_lo(ql), sdesc_of_lo(kl), idS);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-          mma_ss(tbase + kColS, sdesc_sw128(base + L::Q + off, 16, 1024),
-                 sdesc_sw128(ka + off, 16, 1024), idS, kk > 0);
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u) >> 4;
+          mma_ss_c<true>(tbase + kColS, sdesc_of_lo(ql + off), sdesc_of_lo(kl + off), idS);
         }
         mma_commit(bar(L::B_SF));
         mma_commit(bar(L::B_KE + s));
       };
       auto issue_pv = [&](int j) {
         const int s = j & 1;
-        const uint32_t va = base + L::VB + s * L::TILE;
+        const uint32_t vl = opaque(sdesc_lo(base + L::VB + s * L::TILE, L::CHUNK));
+        mma_ts(tbase + kColO, tbase + L::COL_P, sdesc_of_lo(vl), idO, j > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ts(tbase + kColO, tbase + L::COL_P + 8u * kk, sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024),
-                 idO, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 1; kk < kTileN / 16; ++kk)
+          mma_ts_c<true>(tbase + kColO, tbase + L::COL_P + 8u * kk,
+                         sdesc_of_lo(vl + ((2048u * kk) >> 4)), idO);
         mma_commit(bar(L::B_OD));
         mma_commit(bar(L::B_VE + s));
       };

@@ -258,14 +258,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                    : wt2(L::B_SFREE + b, uint32_t((g >> 1) - 1) & 1u, L::B_KFULL + s,
                          uint32_t(g / NST) & 1u);
     };
+    // The issuing lane shares its SM sub-partition with a softmax warp, so
+    // each MMA is issued with as few instructions as possible: descriptors
+    // are built from a 32-bit low word (the high word is one constant), each
+    // K step adds a constant to it, and the accumulate flag is literal.
+    // Same-box A/B on the packed replay: forward 0.97 -> 0.92 ms, dK/dV
+    // 1.97 -> 1.85 ms against descriptors rebuilt per MMA.
     auto issue_s = [&](int g, int qb, bool last_of_unit) {
       const int s = g % NST, b = g & 1;
-      const uint32_t qa = base + L::Q + qb * L::TILE, ka = base + L::K + s * L::TILE;
+      const uint32_t ql = opaque(sdesc_lo(base + L::Q + qb * L::TILE, 16));
+      const uint32_t kl = opaque(sdesc_lo(base + L::K + s * L::TILE, 16));
+      const uint32_t dst = tbase + kColS + 128u * b;
+      mma_ss_c<false>(dst, sdesc_of_lo(ql), sdesc_of_lo(kl), idS);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u;
-        mma_ss(tbase + kColS + 128u * b, sdesc_sw128(qa + off, 16, 1024),
-               sdesc_sw128(ka + off, 16, 1024), idS, kk > 0);
+      for (int kk = 1; kk < D / 16; ++kk) {
+        const uint32_t off = (uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u) >> 4;
+        mma_ss_c<true>(dst, sdesc_of_lo(ql + off), sdesc_of_lo(kl + off), idS);
       }
       mma_commit(bar(L::B_SFULL + b));
       mma_commit(bar(L::B_KEMPTY + s));
@@ -305,11 +313,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (issuer) {
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t va = base + L::V + s * L::TILE;
+            const uint32_t vl = opaque(sdesc_lo(base + L::V + s * L::TILE, L::CHUNK));
+            const uint32_t pa = tbase + kColP + 64u * (g & 1);
+            mma_ts(tbase + kColO, pa, sdesc_of_lo(vl), idO, n > 0 ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk)
-              mma_ts(tbase + kColO, tbase + kColP + 64u * (g & 1) + 8u * kk,
-                     sdesc_sw128(va + 2048u * kk, L::CHUNK, 1024), idO, (n > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 1; kk < kTileN / 16; ++kk)
+              mma_ts_c<true>(tbase + kColO, pa + 8u * kk, sdesc_of_lo(vl + ((2048u * kk) >> 4)), idO);
             mma_commit(bar(L::B_ODONE + (g & 1)));
             mma_commit(bar(L::B_VEMPTY + s));
           }
@@ -535,8 +544,11 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          const CUtensorMap& to, const FwdArgs& a, int n_items, cudaStream_t stream) {
   using L = FwdLayout<D, NST>;
   static_assert(L::ALLOC <= 232448, "forward shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(bda_fwd_kernel<D, NST>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::ALLOC));
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = once_per_device(smem_set, [] {
+    return cudaFuncSetAttribute(bda_fwd_kernel<D, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(L::ALLOC));
+  });
   if (e != cudaSuccess) return e;
   FwdArgs args = a;
   args.n_units = n_items * a.n_groups;

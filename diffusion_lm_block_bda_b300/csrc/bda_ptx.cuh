@@ -264,6 +264,52 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum)
       : "memory");
 }
+// The same MMAs with the accumulate flag fixed at compile time (no predicate
+// set-up on the issuing lane).
+template <bool ACC>
+__device__ __forceinline__ void mma_ss_c(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc) {
+  if (ACC)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc)
+                 : "memory");
+}
+template <bool ACC>
+__device__ __forceinline__ void mma_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                         uint32_t idesc) {
+  if (ACC)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(bdesc), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(bdesc), "r"(idesc)
+                 : "memory");
+}
+
+// Low word of a 128-byte-swizzle descriptor (start address and leading byte
+// offset); the high word (stride 1024 B, version, swizzle mode) is the same
+// for every operand here.  Offsets of whole 16-byte units add to the low word
+// without carry while the address stays inside shared memory (< 2^18).
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t sdesc_of_lo(uint32_t lo) {
+  constexpr uint32_t hi = (1024u >> 4) | (1u << 14) | (2u << 29);
+  return (uint64_t(hi) << 32) | lo;
+}
+// An opaque copy: keeps the compiler from hoisting per-K-step descriptors out
+// of an issue loop (one live register each) in warps with a small budget.
+__device__ __forceinline__ uint32_t opaque(uint32_t x) {
+  uint32_t y;
+  asm volatile("mov.b32 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
