@@ -299,12 +299,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int col = lane + 32 * k;
             const int tok = t0 + (col >> a.lg_hg);
             const int h = h0 + (col & (a.hg - 1));
-            lv[k] = INFINITY;
+            // negated, so the P/dS warps add them in packed fp32 pairs
+            lv[k] = -INFINITY;
             dv[k] = 0.f;
             if (tok < it.lq) {
               const size_t idx = size_t(h) * size_t(a.total_q) + size_t(it.q_row + tok);
-              lv[k] = a.lse[idx] * 1.4426950408889634f;
-              dv[k] = a.D[idx];
+              lv[k] = -(a.lse[idx] * 1.4426950408889634f);
+              dv[k] = -a.D[idx];
             }
           }
         };
@@ -494,7 +495,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int q_hi = min(kq.hi - delta, it.lq);  // local query tokens [kq.lo - delta, q_hi)
     const int q2_lo = kq.lo2 - delta, q2_hi = min(kq.hi2 - delta, it.lq);
     const uint32_t lane_addr = tbase + (uint32_t((warp & 3) * 32) << 16);
-    const float sl2 = a.scale_log2;
+    const uint64_t sl2x2 = f32x2(a.scale_log2, a.scale_log2);
     uint8_t* dsb = gbase + L::DS;
     for (int i = 0; i < n_iter; ++i) {
       const uint32_t ph = uint32_t(i) & 1u;
@@ -534,13 +535,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 l = s_lse4[8 * c + q4];
-          const float p0 = ex2(fmaf(__uint_as_float(r[4 * q4 + 0]), sl2, -l.x));
-          const float p1 = ex2(fmaf(__uint_as_float(r[4 * q4 + 1]), sl2, -l.y));
-          const float p2 = ex2(fmaf(__uint_as_float(r[4 * q4 + 2]), sl2, -l.z));
-          const float p3 = ex2(fmaf(__uint_as_float(r[4 * q4 + 3]), sl2, -l.w));
-          pk[2 * q4] = pack_bf16x2(p0, p1);
-          pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
+          const float4 nl = s_lse4[8 * c + q4];  // -LSE * log2(e)
+          float x0, x1, x2, x3;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[4 * q4 + 0]), __uint_as_float(r[4 * q4 + 1])),
+                                sl2x2, f32x2(nl.x, nl.y)),
+                      x0, x1);
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3])),
+                                sl2x2, f32x2(nl.z, nl.w)),
+                      x2, x3);
+          pk[2 * q4] = pack_bf16x2(ex2(x0), ex2(x1));
+          pk[2 * q4 + 1] = pack_bf16x2(ex2(x2), ex2(x3));
         }
         // Masking clears the bf16 halves of hidden columns.  It sits apart
         // from the exponentials: a branch between them would keep the
@@ -581,17 +585,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto ds_chunk = [&](int c, const uint32_t (&r)[32]) {
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
-          const float4 d0 = s_D4[8 * c + 2 * u4], d1 = s_D4[8 * c + 2 * u4 + 1];
-          const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+          const float4 d0 = s_D4[8 * c + 2 * u4], d1 = s_D4[8 * c + 2 * u4 + 1];  // -D
+          const uint64_t nd[4] = {f32x2(d0.x, d0.y), f32x2(d0.z, d0.w), f32x2(d1.x, d1.y),
+                                  f32x2(d1.z, d1.w)};
           uint32_t pk[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            // dP - D in fp32, rounded to a bf16 pair, times the bf16 pair of
-            // P in one packed multiply (dS is stored as bf16 anyway).
+            // dP - D in fp32 (a packed pair), rounded to a bf16 pair, times
+            // the bf16 pair of P in one packed multiply (dS is stored as bf16
+            // anyway).
             const int cc = 8 * u4 + 2 * j;
-            pk[j] = mul_bf16x2(pp[16 * (c - c0) + 4 * u4 + j],
-                               pack_bf16x2(__uint_as_float(r[cc]) - dd[2 * j],
-                                           __uint_as_float(r[cc + 1]) - dd[2 * j + 1]));
+            float e0, e1;
+            f32x2_split(add_f32x2(f32x2(__uint_as_float(r[cc]), __uint_as_float(r[cc + 1])), nd[j]),
+                        e0, e1);
+            pk[j] = mul_bf16x2(pp[16 * (c - c0) + 4 * u4 + j], pack_bf16x2(e0, e1));
           }
           const int u = 4 * c + u4;
           *reinterpret_cast<uint4*>(dsb + (u >> 3) * L::CHUNK + sw128_offset(kr, u & 7)) =

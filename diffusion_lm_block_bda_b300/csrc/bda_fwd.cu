@@ -392,17 +392,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int j = 0; j < kTileN; ++j)
             if (!(keep[j >> 5] & (1u << (j & 31)))) sv[j] = -INFINITY;
         }
-        // Row max as eight independent chains (a single chain would be 127
-        // dependent steps).
-        float mx8[8];
+        // Row max: three-input max in four independent chains (a single
+        // chain would be 63 dependent steps).
+        float mx4[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) mx8[q] = sv[q];
+        for (int q = 0; q < 4; ++q) mx4[q] = fmaxf(sv[2 * q], sv[2 * q + 1]);
 #pragma unroll
         for (int j = 8; j < kTileN; j += 8)
 #pragma unroll
-          for (int q = 0; q < 8; ++q) mx8[q] = fmaxf(mx8[q], sv[j + q]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int q = 0; q < 4; ++q) mx4[q] = max3f(mx4[q], sv[j + 2 * q], sv[j + 2 * q + 1]);
+        const float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
         const float m_cand = mx * sl2;
         float alpha = 1.f;
         if (m_cand > m_ref + kRescaleThreshold) {
@@ -428,20 +427,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_st32(lane_addr + kColO + 32u * c, rr);
           }
         }
-        float rs[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in four chains
+        // P = 2^(S*scale*log2(e) - m) on column pairs: the scaling FMA and the
+        // row-sum adds run as packed fp32 pairs (two chains of pairs).
+        const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(-m_use, -m_use);
+        uint64_t rs2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < kTileN / 64; ++c) {
           uint32_t pk[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float p0 = ex2(fmaf(sv[64 * c + 2 * j], sl2, -m_use));
-            const float p1 = ex2(fmaf(sv[64 * c + 2 * j + 1], sl2, -m_use));
-            rs[j & 3] += p0 + p1;
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(sv[64 * c + 2 * j], sv[64 * c + 2 * j + 1]), sl2x2, negm2),
+                        x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            rs2[j & 1] = add_f32x2(rs2[j & 1], f32x2(p0, p1));
             pk[j] = pack_bf16x2(p0, p1);
           }
           tmem_st32(lane_addr + kColP + 64u * b + 32u * c, pk);
         }
-        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        float r0, r1, r2, r3;
+        f32x2_split(rs2[0], r0, r1);
+        f32x2_split(rs2[1], r2, r3);
+        l = l * alpha + ((r0 + r1) + (r2 + r3));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(L::B_PFULL));
