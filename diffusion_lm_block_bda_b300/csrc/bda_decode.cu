@@ -492,31 +492,45 @@ __global__ void __launch_bounds__(kTileM) bda_fwd_combine_kernel(const FwdArgs a
   const size_t sstride = size_t(a.n_groups);  // slots of consecutive chunks
   const float* pl = a.part_lse + slot0 * kTileM + r;
   const float4* po = reinterpret_cast<const float4*>(a.part_o) + (slot0 * NQ + size_t(q)) * kTileM + r;
-  // One pass over the chunks with a running maximum (as in an online
-  // softmax): a chunk whose LSE exceeds the maximum so far rescales the sums.
+  // Chunks in batches of 16: every load of a batch is issued before any is
+  // used (the partials sit in L2, so the batch costs about one round trip),
+  // then the batch is merged with a running maximum as in an online softmax.
+  constexpr int kBatch = 16;
   float M = -INFINITY, Lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int s = 0; s < it.n_split; ++s) {
-    const float ls = pl[size_t(s) * sstride * kTileM];
-    const float4 v = po[size_t(s) * sstride * NQ * kTileM];
-    if (ls > M) {
-      const float c = ex2(M - ls);  // 0 while M is -inf
+  for (int s0 = 0; s0 < it.n_split; s0 += kBatch) {
+    float ls[kBatch];
+    float4 v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      ls[j] = s0 + j < it.n_split ? pl[size_t(s0 + j) * sstride * kTileM] : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      v[j] = s0 + j < it.n_split ? po[size_t(s0 + j) * sstride * NQ * kTileM]
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mb = M;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) mb = fmaxf(mb, ls[j]);
+    if (mb > M) {
+      const float c = ex2(M - mb);  // 0 while M is -inf
       Lsum *= c;
       acc.x *= c;
       acc.y *= c;
       acc.z *= c;
       acc.w *= c;
-      M = ls;
+      M = mb;
     }
-    // 0 for a chunk that saw none of this row's keys (its LSE is -inf, and M
-    // may still be -inf, where ls - M would be NaN)
-    const float w = ls > -INFINITY ? ex2(ls - M) : 0.f;
-    Lsum += w;
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      // 0 for a chunk that saw none of this row's keys (its LSE is -inf, and
+      // M may still be -inf, where ls - M would be NaN)
+      const float w = ls[j] > -INFINITY ? ex2(ls[j] - M) : 0.f;
+      Lsum += w;
+      acc.x = fmaf(w, v[j].x, acc.x);
+      acc.y = fmaf(w, v[j].y, acc.y);
+      acc.z = fmaf(w, v[j].z, acc.z);
+      acc.w = fmaf(w, v[j].w, acc.w);
+    }
   }
   const float inv = 1.f / Lsum;
   __nv_bfloat16* orow =

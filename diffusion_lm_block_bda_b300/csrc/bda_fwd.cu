@@ -52,15 +52,19 @@ struct FwdLayout {
   static constexpr uint32_t V = K + NST * TILE;
   static constexpr uint32_t OSTG = V + NST * TILE;  // O staging for the TMA store
   static constexpr uint32_t BAR = OSTG + TILE;
-  // q_full[2], q_empty[2], k_full[NST], k_empty[NST], v_full[NST], v_empty[NST],
-  // s_full[2], s_free[2], p_full, o_done[2] (per P buffer), o_free, drain
+  // q_full[2], q_empty[2], k_full[NST], v_full[NST], s_full[2], s_free[2],
+  // p_full, o_done[2] (per P buffer), o_free, drain.  With two K/V stages
+  // and two S buffers, tile g uses stage g % 2 and buffer g % 2, so the
+  // completion of S(g) frees K stage g % 2 and that of P V(g) frees V stage
+  // g % 2: the producers wait on s_full / o_done (same phases) and the MMA
+  // warp commits each product once (a commit costs the issuing lane tens of
+  // cycles while the softmax warps move data through TMEM).
+  static_assert(NST == 2, "K/V stages are released through the S and O barriers");
   static constexpr int B_QFULL = 0;
   static constexpr int B_QEMPTY = 2;
   static constexpr int B_KFULL = 4;
-  static constexpr int B_KEMPTY = B_KFULL + NST;
-  static constexpr int B_VFULL = B_KEMPTY + NST;
-  static constexpr int B_VEMPTY = B_VFULL + NST;
-  static constexpr int B_SFULL = B_VEMPTY + NST;
+  static constexpr int B_VFULL = B_KFULL + NST;
+  static constexpr int B_SFULL = B_VFULL + NST;
   static constexpr int B_SFREE = B_SFULL + 2;
   static constexpr int B_PFULL = B_SFREE + 2;
   static constexpr int B_ODONE = B_PFULL + 1;
@@ -127,9 +131,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int s = 0; s < NST; ++s) {
       mbar_init(bar(L::B_KFULL + s), 1);
-      mbar_init(bar(L::B_KEMPTY + s), 1);
       mbar_init(bar(L::B_VFULL + s), 1);
-      mbar_init(bar(L::B_VEMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::B_SFULL + b), 1);
@@ -189,7 +191,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int nq[2] = {0, 0}, ncopy[NST];  // copies issued per barrier (abort drain)
       for (int s = 0; s < NST; ++s) ncopy[s] = 0;
       const int b_full = kprod ? L::B_KFULL : L::B_VFULL;
-      const int b_empty = kprod ? L::B_KEMPTY : L::B_VEMPTY;
+      // stage s of tile g is free once S(g - 2) (K) or P V(g - 2) (V) completed
+      const int b_empty = kprod ? L::B_SFULL : L::B_ODONE;
       const CUtensorMap* tm = kprod ? &tm_k : &tm_v;
       const uint32_t ring = base + (kprod ? L::K : L::V);
       bool ok = true;
@@ -275,8 +278,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t off = (uint32_t(kk >> 2) * L::CHUNK + uint32_t(kk & 3) * 32u) >> 4;
         mma_ss_c<true>(dst, sdesc_of_lo(ql + off), sdesc_of_lo(kl + off), idS);
       }
-      mma_commit(bar(L::B_SFULL + b));
-      mma_commit(bar(L::B_KEMPTY + s));
+      mma_commit(bar(L::B_SFULL + b));  // also frees K stage s (s == b)
       if (last_of_unit) mma_commit(bar(L::B_QEMPTY + qb));
     };
     bool go = true;
@@ -319,8 +321,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
             for (int kk = 1; kk < kTileN / 16; ++kk)
               mma_ts_c<true>(tbase + kColO, pa + 8u * kk, sdesc_of_lo(vl + ((2048u * kk) >> 4)), idO);
-            mma_commit(bar(L::B_ODONE + (g & 1)));
-            mma_commit(bar(L::B_VEMPTY + s));
+            mma_commit(bar(L::B_ODONE + (g & 1)));  // also frees V stage s
           }
         }
       }
