@@ -4,7 +4,11 @@ C-ABI binding, run the fp64 oracle on the same seeded bf16 inputs, compare.
 Tolerances (written here, used by every parity test):
   O    : max-abs <= 2e-2 and relative L2 <= 5e-3
   LSE  : max_i |LSE - LSE*| / max(|LSE*_i|, 1) <= 1e-3
-  dQ, dK, dV : relative L2 <= 1e-2 each
+  dQ, dK, dV : relative L2 <= 1e-2 each, the reference norm floored at
+               1e-3 * sqrt(elements) (an RMS of 1e-3): relative L2 has no
+               meaning for a zero reference, and a gradient can be exactly
+               zero (a one-token sequence's softmax over a single key has
+               zero derivative) while fp32 rounding of dP - D leaves ~1e-7.
 """
 import numpy as np
 import torch
@@ -12,7 +16,7 @@ import torch
 import oracle
 from diffusion_lm_block_bda_b300 import Attention, Problem, workloads as W
 
-O_MAXABS, O_REL, LSE_REL, GRAD_REL = 2e-2, 5e-3, 1e-3, 1e-2
+O_MAXABS, O_REL, LSE_REL, GRAD_REL, GRAD_RMS_FLOOR = 2e-2, 5e-3, 1e-3, 1e-2, 1e-3
 
 
 def rel_l2(x, ref):
@@ -42,9 +46,10 @@ def check_lse(lse, ref, what=""):
 
 
 def check_grad(g, ref, name, what=""):
-    g = np.asarray(g, np.float64)
+    g, ref = np.asarray(g, np.float64), np.asarray(ref, np.float64)
     assert np.isfinite(g).all(), f"{what}: non-finite {name}"
-    e = rel_l2(g, ref)
+    floor = GRAD_RMS_FLOOR * np.sqrt(max(ref.size, 1))
+    e = float(np.linalg.norm((g - ref).ravel()) / max(np.linalg.norm(ref.ravel()), floor))
     assert e <= GRAD_REL, f"{what}: {name} rel-L2 {e:.3e}"
     return e
 
