@@ -259,3 +259,20 @@ def test_long_block_causal_c5():
     compare_sampled(w, inp, got, seqs=[0], kv_heads=(0, 1),
                     qrows_fn=lambda n: _sample_rows(n, 24), krows_fn=lambda n: keys)
     check_sum_rules(w, inp, got)
+
+
+def test_largest_sequence_128k():
+    """One 131,072-token sequence, block 128, Hq=32, Hkv=8, d=128: every
+    tensor is 4x that of the long-sequence workload and the fp32 dQ
+    accumulator spans 2 GiB, so no byte offset or element index may wrap at
+    32 bits.  O/LSE/dQ on sampled query rows, dK/dV on the last keys (few
+    query rows see them, so the oracle stays cheap) and on a key tile in the
+    middle, plus the sum rules over the whole sequence."""
+    L = 131072
+    w = W.custom(BC, 128, 32, 8, 128, [L], name="block_causal_128k")
+    inp = W.make_inputs(w, seed=7)
+    got = gpu_run(w, inp)
+    keys = list(range(L - 640, L - 512)) + _tail_keys(L, 96)
+    compare_sampled(w, inp, got, seqs=[0], kv_heads=(7, 8),
+                    qrows_fn=lambda n: _sample_rows(n, 16), krows_fn=lambda n: keys)
+    check_sum_rules(w, inp, got)
