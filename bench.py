@@ -689,20 +689,22 @@ def main():
     out["bwd_tflops"] = bwd_flops / (sum(stage_ms[2:]) * 1e-3) / 1e12
     if e2e is not None:
         out["e2e"] = e2e
-    if not args.no_decode:
+    # The side measurements and the CPU baseline belong to the one-GPU line;
+    # a multi-GPU line carries the data-parallel step only.
+    if not args.no_decode and world == 1:
         try:
             out["decode"] = decode_measurement(bda, dev, stream, hbm)
         except Exception as e:  # a side measurement: the main line is printed regardless
             torch.cuda.synchronize()
             out["decode"] = {"error": f"{type(e).__name__}: {e}"}
-    if not args.no_side:
+    if not args.no_side and world == 1:
         for key, name, reps in (("staircase", "c4", 20), ("long", "c5", 5)):
             try:
                 out[key] = side_measurement(bda, dev, stream, name, peak_burst, reps)
             except Exception as e:  # a side measurement: the main line is printed regardless
                 torch.cuda.synchronize()
                 out[key] = {"error": f"{type(e).__name__}: {e}"}
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(w, inp)
     print(json.dumps(out), flush=True)
 
