@@ -246,7 +246,7 @@ bda_status bda_attn_fwd(const bda_problem* prob, const bda_mask_desc* mask, cons
   if (!make_thd_map(&tq, q, s.d, s.hq, s.total_q, s.hg, s.tok) ||
       !make_thd_map(&tk, k, s.d, s.hkv, s.total_k, 1, kTileN) ||
       !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN) ||
-      !make_thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok))
+      !make_thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok / 4))
     return tensor_map_error();
   const FwdArgs a = make_fwd_args(s, plan_ptr(ws), /*with_bwd=*/true, o, lse,
                                   reinterpret_cast<uint32_t*>(ws), static_cast<uint8_t*>(ws));

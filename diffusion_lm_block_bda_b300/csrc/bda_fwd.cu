@@ -38,7 +38,6 @@ namespace {
 
 constexpr int kFwdThreads = 256;
 constexpr uint32_t kMmaGate = 1;     // named barrier between the MMA warp and its waiter
-constexpr uint32_t kEpiBarrier = 2;  // named barrier of the softmax warps (epilogue)
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // P0 at kColP, P1 at kColP + 64
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
 
@@ -343,6 +342,84 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     Unit nx{};  // the next unit's descriptor, fetched one unit ahead
     int u = unit_of(0, n_units);
     if (u >= 0) nx = load_unit(u);
+    // A finished unit's epilogue: O out of TMEM (then the next unit's first
+    // P V may overwrite it), O / l and LSE to global memory.  It runs after
+    // the next unit's first P is out: by then its last P V has completed, and
+    // the MMA warp has had that unit's first products to work on meanwhile.
+    struct Pend {
+      int head0, q_row, q_len, gl;  // the unit's head group, rows, last key tile
+      float l, m;                   // its row sum and reference max
+    };
+    auto epilogue = [&](const Pend& pd) -> bool {
+      if (!mbar_wait_warp(wc, bar(L::B_ODONE + (pd.gl & 1)), uint32_t(pd.gl >> 1) & 1u))
+        return false;
+        tc_fence_after();
+        uint32_t ov[D / 32][32];
+  #pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_addr + kColO + 32u * c, ov[c]);
+  #pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld_wait(ov[c]);
+        tc_fence_before();
+        mbar_arrive(bar(L::B_OFREE));
+        const float inv_l = 1.f / pd.l;
+        const bool row_valid = t_local < pd.q_len;
+        if (pd.q_len == (kTileM >> a.lg_hg)) {
+          // Whole tile: each warp's 32 rows (a quarter of the tile's tokens x
+          // its hg heads) go to swizzled shared memory (conflict-free) and the
+          // warp's lane 0 has the TMA write them (a store from each thread
+          // would hit 32 rows per instruction).  The warp's previous store must
+          // have read its part of the staging buffer first.
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+  #pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t pk[16];
+  #pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[j] = pack_bf16x2(__uint_as_float(ov[c][2 * j]) * inv_l,
+                                  __uint_as_float(ov[c][2 * j + 1]) * inv_l);
+  #pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(gbase + L::OSTG + (c >> 1) * L::CHUNK +
+                                        sw128_offset(r, 4 * (c & 1) + j)) =
+                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int tok_w = kTileM >> (a.lg_hg + 2);  // tokens of one warp's 32 rows
+            for (int c = 0; c < L::CH; ++c)
+              tma_store_3d(&tm_o, base + L::OSTG + c * L::CHUNK + uint32_t(warp) * 4096u, 64 * c,
+                           pd.head0, pd.q_row + warp * tok_w);
+            bulk_commit();
+          }
+        } else if (row_valid) {
+          // The sequence's last, partial tile: the box would spill into the
+          // next sequence's rows, so each thread stores its own row.
+          __nv_bfloat16* orow =
+              a.o + (size_t(pd.q_row + t_local) * a.hq + size_t(pd.head0 + hh)) * size_t(D);
+  #pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t pk[16];
+  #pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[j] = pack_bf16x2(__uint_as_float(ov[c][2 * j]) * inv_l,
+                                  __uint_as_float(ov[c][2 * j + 1]) * inv_l);
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+  #pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
+        }
+        if (row_valid) {
+          const float lse2 = pd.m + log2f(pd.l);
+          a.lse[size_t(pd.head0 + hh) * size_t(a.total_q) + size_t(pd.q_row + t_local)] =
+              lse2 * 0.69314718055994530942f;
+        }
+      return true;
+    };
+    Pend pend{};
+    bool have_pend = false;
     for (int k = 0; ok && u >= 0; ++k) {
       const Unit x = nx;
       u = unit_of(k + 1, n_units);
@@ -453,79 +530,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(L::B_PFULL));
-      }
-      // Epilogue: O out of TMEM (then the next unit's first P V may
-      // overwrite it), O / l and LSE to global memory.  The four warps meet
-      // at a named barrier that also carries their verdicts, so a failed
-      // wait anywhere stops all of them here together.
-      const int gl = g - 1;  // the unit's last key tile
-      bool good = ok && mbar_wait_warp(wc, bar(L::B_ODONE + (gl & 1)), uint32_t(gl >> 1) & 1u);
-      good = named_bar_and(kEpiBarrier, 128, good);
-      if (!good) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t ov[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_addr + kColO + 32u * c, ov[c]);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld_wait(ov[c]);
-      tc_fence_before();
-      mbar_arrive(bar(L::B_OFREE));
-      const float inv_l = 1.f / l;
-      if (it.q_len == (kTileM >> a.lg_hg)) {
-        // Whole tile: rows go to swizzled shared memory (conflict-free) and
-        // the TMA writes the tile (a store from each thread would hit 32
-        // rows per instruction).  The previous store must have read the
-        // staging buffer first.
-        if (r == 0) bulk_wait_read<0>();
-        named_bar_sync(kEpiBarrier, 128);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(__uint_as_float(ov[c][2 * j]) * inv_l,
-                                __uint_as_float(ov[c][2 * j + 1]) * inv_l);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(gbase + L::OSTG + (c >> 1) * L::CHUNK +
-                                      sw128_offset(r, 4 * (c & 1) + j)) =
-                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(kEpiBarrier, 128);
-        if (r == 0) {
-          for (int c = 0; c < L::CH; ++c)
-            tma_store_3d(&tm_o, base + L::OSTG + c * L::CHUNK, 64 * c, x.head0, it.q_row);
-          bulk_commit();
-        }
-      } else if (row_valid) {
-        // The sequence's last, partial tile: the box would spill into the
-        // next sequence's rows, so each thread stores its own row.
-        __nv_bfloat16* orow =
-            a.o + (size_t(it.q_row + t_local) * a.hq + size_t(x.head0 + hh)) * size_t(D);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(__uint_as_float(ov[c][2 * j]) * inv_l,
-                                __uint_as_float(ov[c][2 * j + 1]) * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        if (n == 0 && have_pend) {  // the previous unit's epilogue
+          have_pend = false;
+          if (!epilogue(pend)) {
+            ok = false;
+            break;
+          }
         }
       }
-      if (row_valid) {
-        const float lse2 = m_ref + log2f(l);
-        a.lse[size_t(x.head0 + hh) * size_t(a.total_q) + size_t(it.q_row + t_local)] =
-            lse2 * 0.69314718055994530942f;
-      }
+      if (!ok) break;
+      pend = Pend{x.head0, it.q_row, it.q_len, g - 1, l, m_ref};
+      have_pend = true;
     }
-    if (r == 0) bulk_wait_all();  // the last O stores complete before the CTA exits
+    if (ok && have_pend) ok = epilogue(pend);
+    if (lane == 0) bulk_wait_all();  // the last O stores complete before the CTA exits
   }
 
   tc_fence_before();

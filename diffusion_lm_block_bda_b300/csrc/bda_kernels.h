@@ -86,7 +86,7 @@ FwdArgs make_fwd_args(const Shape& s, const uint8_t* plan, bool with_bwd, void* 
 BwdArgs make_bwd_args(const Shape& s, const uint8_t* plan, const float* lse, const float* D,
                       void* dk, void* dv, uint32_t* status);
 
-// to: map over O laid out like Q (box 64 x hg x tok, 128-byte swizzle); whole
+// to: map over O laid out like Q (box 64 x hg x tok / 4: one warp's 32 rows, 128-byte swizzle); whole
 // query tiles are written through it.
 cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, int n_items,

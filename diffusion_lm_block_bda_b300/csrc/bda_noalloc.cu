@@ -117,7 +117,7 @@ bda_status bda_attn_fwd_noalloc(const bda_problem* prob, const bda_mask_desc* ma
   if (!make_thd_map(&tq, q, s.d, s.hq, s.total_q, s.hg, s.tok) ||
       !make_thd_map(&tk, k, s.d, s.hkv, s.total_k, 1, kTileN) ||
       !make_thd_map(&tv, v, s.d, s.hkv, s.total_k, 1, kTileN) ||
-      !make_thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok)) {
+      !make_thd_map(&to, o, s.d, s.hq, s.total_q, s.hg, s.tok / 4)) {
     note_cuda_error("cuTensorMapEncodeTiled failed");
     return BDA_ERR_CUDA;
   }
