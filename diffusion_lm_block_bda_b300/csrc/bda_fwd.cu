@@ -52,7 +52,14 @@ struct FwdLayout {
   static constexpr uint32_t OSTG = V + NST * TILE;  // O staging for the TMA store
   static constexpr uint32_t BAR = OSTG + TILE;
   // q_full[2], q_empty[2], k_full[NST], v_full[NST], s_full[2], s_free[2],
-  // p_full, o_done[2] (per P buffer), o_free, drain.  With two K/V stages
+  // p_full[2], o_done[2] (per P buffer), o_free[2] (per unit parity), drain.
+  // Barriers that all softmax threads arrive on come in pairs: the S and P
+  // buffers are double, so one softmax warp may finish tile g+1 before
+  // another has finished tile g, and its arrivals must not count towards
+  // tile g's phase (one p_full barrier let P V(g) start without the slow
+  // warp's rows of P).  A warp reaches tile g+2 only after P V(g) completed,
+  // which needs every warp's P(g), and the first P V of unit k+1 needs
+  // every warp's o_free arrival for unit k, so two of each suffice.  With two K/V stages
   // and two S buffers, tile g uses stage g % 2 and buffer g % 2, so the
   // completion of S(g) frees K stage g % 2 and that of P V(g) frees V stage
   // g % 2: the producers wait on s_full / o_done (same phases) and the MMA
@@ -66,9 +73,9 @@ struct FwdLayout {
   static constexpr int B_SFULL = B_VFULL + NST;
   static constexpr int B_SFREE = B_SFULL + 2;
   static constexpr int B_PFULL = B_SFREE + 2;
-  static constexpr int B_ODONE = B_PFULL + 1;
+  static constexpr int B_ODONE = B_PFULL + 2;
   static constexpr int B_OFREE = B_ODONE + 2;
-  static constexpr int B_DRAIN = B_OFREE + 1;
+  static constexpr int B_DRAIN = B_OFREE + 2;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr uint32_t MISC = BAR + 8 * NBAR;
   static constexpr uint32_t BYTES = MISC + 16;
@@ -135,10 +142,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::B_SFULL + b), 1);
       mbar_init(bar(L::B_SFREE + b), 128);
+      mbar_init(bar(L::B_PFULL + b), 128);
       mbar_init(bar(L::B_ODONE + b), 1);
+      mbar_init(bar(L::B_OFREE + b), 128);
     }
-    mbar_init(bar(L::B_PFULL), 128);
-    mbar_init(bar(L::B_OFREE), 128);
     mbar_init(bar(L::B_DRAIN), 1);
     fence_mbar_init();
   }
@@ -307,9 +314,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // O += P V; the unit's first product overwrites O, so the previous
         // unit's epilogue must have read it out.
         const int s = g % NST;
-        if (!(go = gate(issuer || (wt2(L::B_VFULL + s, uint32_t(g / NST) & 1u, L::B_PFULL,
-                                       uint32_t(g) & 1u) &&
-                                   (n > 0 || k == 0 || wt(L::B_OFREE, uint32_t(k - 1) & 1u))))))
+        if (!(go = gate(issuer || (wt2(L::B_VFULL + s, uint32_t(g / NST) & 1u, L::B_PFULL + (g & 1),
+                                       uint32_t(g >> 1) & 1u) &&
+                                   (n > 0 || k == 0 ||
+                                    wt(L::B_OFREE + ((k - 1) & 1), uint32_t((k - 1) >> 1) & 1u))))))
           break;
         if (issuer) {
           tc_fence_after();
@@ -347,8 +355,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // the next unit's first P is out: by then its last P V has completed, and
     // the MMA warp has had that unit's first products to work on meanwhile.
     struct Pend {
-      int head0, q_row, q_len, gl;  // the unit's head group, rows, last key tile
-      float l, m;                   // its row sum and reference max
+      int head0, q_row, q_len, gl, k;  // the unit's head group, rows, last key tile, index
+      float l, m;                      // its row sum and reference max
     };
     auto epilogue = [&](const Pend& pd) -> bool {
       if (!mbar_wait_warp(wc, bar(L::B_ODONE + (pd.gl & 1)), uint32_t(pd.gl >> 1) & 1u))
@@ -360,7 +368,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   #pragma unroll
         for (int c = 0; c < D / 32; ++c) tmem_ld_wait(ov[c]);
         tc_fence_before();
-        mbar_arrive(bar(L::B_OFREE));
+        mbar_arrive(bar(L::B_OFREE + (pd.k & 1)));
         const float inv_l = 1.f / pd.l;
         const bool row_valid = t_local < pd.q_len;
         if (pd.q_len == (kTileM >> a.lg_hg)) {
@@ -529,7 +537,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         l = l * alpha + ((r0 + r1) + (r2 + r3));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(L::B_PFULL));
+        mbar_arrive(bar(L::B_PFULL + b));
         if (n == 0 && have_pend) {  // the previous unit's epilogue
           have_pend = false;
           if (!epilogue(pend)) {
@@ -539,7 +547,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
       if (!ok) break;
-      pend = Pend{x.head0, it.q_row, it.q_len, g - 1, l, m_ref};
+      pend = Pend{x.head0, it.q_row, it.q_len, g - 1, k, l, m_ref};
       have_pend = true;
     }
     if (ok && have_pend) ok = epilogue(pend);
