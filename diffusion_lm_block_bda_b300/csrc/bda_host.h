@@ -36,6 +36,9 @@ struct Shape {
 // writes half as many partial results.
 constexpr int kSplitMaxUnits = 74;
 constexpr int kSplitTargetUnits = 74;
+// The backward's last wave, ordered longest-first: one dK/dV CTA per SM of a
+// B300 (148 SMs).
+constexpr int kTailWaveCtas = 148;
 
 // Validates the problem and mask; fills `s`.  Host-only, launches nothing.
 // A multi-block staircase whose non-empty groups are not in block order

@@ -370,6 +370,15 @@ void build_plan(const bda_problem* p, const bda_mask_desc* m, const Shape& s, ui
     }
     return a.work > b.work;
   });
+  // The last wave goes longest-first across sequences.  The block scheduler
+  // hands out CTAs in grid order (item-major, hkv CTAs per item), so with
+  // the tail in sequence order the last sequence's longest key tiles would
+  // start last (the staircase replay's dK/dV: 148 -> 132 query tiles on the
+  // busiest SM in a list schedule over 148 SMs).  The wave's few items span
+  // two or three sequences, whose Q, dO and dQ rows still fit in L2.
+  const size_t n_tail = std::min(bw.size(), size_t((kTailWaveCtas + s.hkv - 1) / s.hkv));
+  std::stable_sort(bw.end() - std::ptrdiff_t(n_tail), bw.end(),
+                   [](const BwdItem& a, const BwdItem& b) { return a.work > b.work; });
   // Split-forward units, in the forward items' (longest-first) order: each
   // item's key tiles cut into n_split nearly equal chunks of about split_c.
   DecItem* dec = reinterpret_cast<DecItem*>(out + plan_dec_offset(s, with_bwd));
