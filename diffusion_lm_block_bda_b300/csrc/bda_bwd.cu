@@ -175,10 +175,13 @@ __device__ __forceinline__ void expect_tx(uint32_t bar, uint32_t bytes) {
 // Per (128-key tile, KV head) CTA; loops over the query tiles i that see the
 // key tile.  MMA issue order per query tile (one thread):
 //   dV   += P_i^T dO_i      A = P^T from TMEM, after P_i^T is stored    -> DVDONE
-//   S^T_{i+1} = K Q_{i+1}^T after dV_i has read P_i^T (same columns)    -> SFULL
 //   dQ_i  = dS_i K          after dS_i^T is in smem                     -> DQFULL
+//   S^T_{i+1} = K Q_{i+1}^T after dV_i has read P_i^T (same columns)    -> SFULL
 //   dK   += dS_i^T Q_i                                                   -> DSCONS, QEMPTY
 //   dP^T_{i+1} = V dO_{i+1}^T after dQ_i left TMEM and dO_{i+1} landed  -> DPFULL
+// dQ_i sits between dV_i and S^T_{i+1}, so the tensor pipe has work while
+// the issuer waits for dV_i to complete, and the dQ read-out has S^T_{i+1}
+// and dK_i to hide behind before dP^T_{i+1} needs its columns.
 // MMAs into different accumulators are not ordered by the hardware, so every
 // reuse of a TMEM region or smem buffer waits for a commit of its readers.
 // The dQ partial of each query tile leaves TMEM through shared memory and is
@@ -427,17 +430,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_commit(bar(L::B_DVDONE));
             }
           }
-          // next S^T once its Q is in and dV has read P^T out of the S^T columns
-          if (i + 1 < n_iter) {
-            if (!(go = gate(issuer || wt2(L::B_QFULL + (st ^ 1), uint32_t((i + 1) >> 1) & 1u,
-                                          L::B_DVDONE, ph))))
-              break;
-            if (issuer) {
-              tc_fence_after();
-              if (lane == 0) issue_s(i + 1);
-            }
-          }
-          // dQ = dS K, then dK += dS^T Q
+          // dQ = dS K right behind dV, so the wait of the next S^T for dV to
+          // complete overlaps it
           if (!(go = gate(issuer || wt(L::B_DSFULL, ph)))) break;
           if (issuer) {
             tc_fence_after();
@@ -450,6 +444,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_ss_c<true>(tbase + kColDP, sdesc_of_lo(sl + ((2048u * kk) >> 4)),
                                sdesc_of_lo(kl + ((2048u * kk) >> 4)), idDQ);
               mma_commit(bar(L::B_DQFULL));
+            }
+          }
+          // next S^T once its Q is in and dV has read P^T out of the S^T columns
+          if (i + 1 < n_iter) {
+            if (!(go = gate(issuer || wt2(L::B_QFULL + (st ^ 1), uint32_t((i + 1) >> 1) & 1u,
+                                          L::B_DVDONE, ph))))
+              break;
+            if (issuer) {
+              tc_fence_after();
+              if (lane == 0) issue_s(i + 1);
+            }
+          }
+          // dK += dS^T Q (dS^T is already in: its gate opened for dQ)
+          if (issuer) {
+            tc_fence_after();
+            if (lane == 0) {
               const uint32_t tl = opaque(sdesc_lo(base + L::DS, 16));
               const uint32_t ql = opaque(sdesc_lo(base + L::Q + st * L::TILE, L::CHUNK));
               mma_ss(tbase + kColDK, sdesc_of_lo(tl), sdesc_of_lo(ql), idAcc, i > 0 ? 1u : 0u);
