@@ -1,4 +1,4 @@
-"""GPU parity on random small layouts: block-causal (with and without fewer
+"""GPU parity on 120 random small layouts: block-causal (with and without fewer
 queries than keys), single-block staircase and multi-block staircase, drawn
 from one seeded generator over block sizes 1..256, GQA ratios 1..8, head_dim
 64 and 128, ragged and empty sequences.  Each case goes through both forward
@@ -20,7 +20,7 @@ from _parity import compare_full, gpu_run, oracle_full
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 24
+N_CASES = 120
 
 
 @pytest.fixture(scope="module", autouse=True)
