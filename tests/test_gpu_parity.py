@@ -69,6 +69,10 @@ EDGE = [
     (SC, 32, 8, 2, 128, [1536], None, [1024]),                      # one staircase trajectory
     (SC, 16, 8, 2, 64, [96], None, [0]),                            # copies only, d = 64
     (SC, 128, 4, 1, 128, [640], None, [256]),                       # copies of 128 tokens
+    (BC, 32, 16, 1, 128, [300, 77], None, None),                    # G = 16: 8-token tiles
+    (BC, 16, 32, 1, 64, [200, 9], None, None),                      # G = 32: two head groups per KV head
+    (SC, 32, 12, 2, 128, [264], None, [72]),                        # G = 6 (head groups of 2)
+    (BC, 16, 6, 2, 128, [130, 31], None, None),                     # G = 3 (head groups of 1)
 ]
 
 
