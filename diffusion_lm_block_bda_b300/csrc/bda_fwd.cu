@@ -16,9 +16,8 @@
 // product overlap the current unit's last softmax and epilogue.  Roles:
 //   warp 4        TMA producer of Q (two buffers) and K (NST-stage ring)
 //   warp 7        TMA producer of V (NST-stage ring)
-//   warp 5        tcgen05 MMA issuer (one thread): S = Q K^T into TMEM
-//                 (double buffered), O += P V with P read from TMEM
-//   warp 6        waits on the MMAs' dependencies and gates warp 5
+//   warp 6        tcgen05 issuer of S = Q K^T into TMEM (double buffered)
+//   warp 5        tcgen05 issuer of O += P V, P read from TMEM
 //   warps 0..3    softmax: thread r owns TMEM lane r = query row r; masks
 //                 PARTIAL tiles from block indices, online max/sum, writes P
 //                 as bf16 into TMEM, rescales O when the max grows by more
@@ -37,7 +36,6 @@ namespace bda {
 namespace {
 
 constexpr int kFwdThreads = 256;
-constexpr uint32_t kMmaGate = 1;     // named barrier between the MMA warp and its waiter
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // P0 at kColP, P1 at kColP + 64
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
 
@@ -146,7 +144,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar(L::B_ODONE + b), 1);
       mbar_init(bar(L::B_OFREE + b), 128);
     }
-    mbar_init(bar(L::B_DRAIN), 1);
+    mbar_init(bar(L::B_DRAIN), 2);  // one commit from each MMA issuer
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -245,15 +243,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == 5 || warp == 6) {
     // ----------------------------------------------------------------- MMA
-    // Warp 5 issues every MMA (lane 0); warp 6 waits on the mbarriers each
-    // product depends on and opens a named-barrier gate for it.  An mbarrier
-    // wait issued right behind a batch of MMAs queues behind them (hundreds
-    // of cycles even on a completed phase), while a named barrier costs a
-    // few cycles, so the issuing warp only ever meets named barriers.  The
-    // gate also carries the waiter's verdict: a failed wait stops both warps
-    // at the same gate.
-    const bool issuer = warp == 5;
-    auto gate = [&](bool wait_ok) -> bool { return named_bar_and(kMmaGate, 64, wait_ok); };
+    // Two issuers, each waiting on the mbarriers of its own products: warp 6
+    // issues every S = Q K^T, warp 5 every O += P V (lane 0).  A tcgen05.mma
+    // holds its issuing thread until the pipe accepts it, so with one issuer
+    // S(g+1) could not start before all of P V(g-1) was issued, and that
+    // chain (P out -> P V issue -> next S issue -> S done -> softmax) set the
+    // tile period.  The two products share no operand (separate TMEM buffers,
+    // K and V stages of their own) and each commit tracks only its own
+    // thread's MMAs.
+    const bool s_issuer = warp == 6;
     auto wt = [&](int b, uint32_t parity) -> bool { return mbar_wait_warp(wc, bar(b), parity); };
     auto wt2 = [&](int b1, uint32_t p1, int b2, uint32_t p2) -> bool {
       return mbar_wait2_warp(wc, bar(b1), p1, bar(b2), p2);
@@ -297,29 +295,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       u = unit_of(k + 1, n_units);
       if (u >= 0) nx = load_unit(u);
       const int qb = k & 1;
-      if (!(go = gate(issuer || (wt(L::B_QFULL + qb, uint32_t(k >> 1) & 1u) && s_ready(g)))))
-        break;
-      if (issuer) {
-        tc_fence_after();
-        if (lane == 0) issue_s(g, qb, x.n_tiles == 1);
-      }
-      for (int n = 0; n < x.n_tiles; ++n, ++g) {
-        if (n + 1 < x.n_tiles) {
-          if (!(go = gate(issuer || s_ready(g + 1)))) break;
-          if (issuer) {
-            tc_fence_after();
-            if (lane == 0) issue_s(g + 1, qb, n + 2 == x.n_tiles);
-          }
+      if (s_issuer) {
+        // S(g) once its Q (first tile of a unit), its K and its S buffer are in
+        for (int n = 0; n < x.n_tiles; ++n, ++g) {
+          if (!(go = (n > 0 || wt(L::B_QFULL + qb, uint32_t(k >> 1) & 1u)) && s_ready(g))) break;
+          tc_fence_after();
+          if (lane == 0) issue_s(g, qb, n + 1 == x.n_tiles);
         }
+      } else {
         // O += P V; the unit's first product overwrites O, so the previous
         // unit's epilogue must have read it out.
-        const int s = g % NST;
-        if (!(go = gate(issuer || (wt2(L::B_VFULL + s, uint32_t(g / NST) & 1u, L::B_PFULL + (g & 1),
-                                       uint32_t(g >> 1) & 1u) &&
-                                   (n > 0 || k == 0 ||
-                                    wt(L::B_OFREE + ((k - 1) & 1), uint32_t((k - 1) >> 1) & 1u))))))
-          break;
-        if (issuer) {
+        for (int n = 0; n < x.n_tiles; ++n, ++g) {
+          const int s = g % NST;
+          if (!(go = wt2(L::B_VFULL + s, uint32_t(g / NST) & 1u, L::B_PFULL + (g & 1),
+                         uint32_t(g >> 1) & 1u) &&
+                     (n > 0 || k == 0 ||
+                      wt(L::B_OFREE + ((k - 1) & 1), uint32_t((k - 1) >> 1) & 1u))))
+            break;
           tc_fence_after();
           if (lane == 0) {
             const uint32_t vl = opaque(sdesc_lo(base + L::V + s * L::TILE, L::CHUNK));
@@ -333,8 +325,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
     }
-    if (issuer && lane == 0) {
-      // Every MMA issued above completes before TMEM can be released.
+    if (lane == 0) {
+      // Every MMA this thread issued completes before TMEM can be released
+      // (the drain barrier takes one commit from each issuer).
       mma_commit(bar(L::B_DRAIN));
       drain_wait(wc, bar(L::B_DRAIN), 0);
     }
