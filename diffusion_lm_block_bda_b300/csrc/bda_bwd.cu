@@ -27,8 +27,8 @@
 //   warps 4..7   softmax, query columns [64, 128), then the dV epilogue
 //   warps 8..11  dQ readout + staging for the TMA reduce
 //   warp 12      producer: K/V once, then Q, dO (TMA) and LSE, D per query tile
-//   warp 13      MMA issuer (one thread)
-//   warp 14      waits on the MMAs' dependencies and gates warp 13
+//   warp 13      MMA issuer of dV, dQ and dK (one thread)
+//   warp 14      MMA issuer of S^T and dP^T (one thread)
 //   warp 15      idle
 // P and dS are elementwise in (key, query) given LSE and D, so the two
 // softmax warpgroups split each tile's columns with no exchange; two warps
@@ -127,7 +127,6 @@ constexpr int kRegsSoftmax = 144, kRegsDq = 160, kRegsOther = 64, kRegsLaunch = 
 static_assert(2 * kRegsSoftmax + kRegsDq + kRegsOther == 4 * kRegsLaunch, "register split");
 constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
 constexpr uint32_t kDqBarrier = 1;  // named barrier of the dQ warpgroup (warps 4..7)
-constexpr uint32_t kMmaGate = 2;    // named barrier between the MMA warp and its waiter
 
 // Shared memory (D = 128): K | V | Q x2 | dO | dS^T | dQ staging x2 | LSE x2 |
 // D x2 | barriers = 226.1 KB, so there is no slack to align the base by hand:
@@ -173,15 +172,14 @@ __device__ __forceinline__ void expect_tx(uint32_t bar, uint32_t bytes) {
 }
 
 // Per (128-key tile, KV head) CTA; loops over the query tiles i that see the
-// key tile.  MMA issue order per query tile (one thread):
-//   dV   += P_i^T dO_i      A = P^T from TMEM, after P_i^T is stored    -> DVDONE
-//   dQ_i  = dS_i K          after dS_i^T is in smem                     -> DQFULL
-//   S^T_{i+1} = K Q_{i+1}^T after dV_i has read P_i^T (same columns)    -> SFULL
-//   dK   += dS_i^T Q_i                                                   -> DSCONS, QEMPTY
-//   dP^T_{i+1} = V dO_{i+1}^T after dQ_i left TMEM and dO_{i+1} landed  -> DPFULL
-// dQ_i sits between dV_i and S^T_{i+1}, so the tensor pipe has work while
-// the issuer waits for dV_i to complete, and the dQ read-out has S^T_{i+1}
-// and dK_i to hide behind before dP^T_{i+1} needs its columns.
+// key tile.  Two threads issue the MMAs, per query tile i:
+//   warp 14 (what the P/dS warps consume):
+//     S^T_i = K Q_i^T      after Q_i landed and dV_{i-1} read P^T_{i-1}    -> SFULL
+//     dP^T_i = V dO_i^T    after dO_i landed and dQ_{i-1} left TMEM       -> DPFULL
+//   warp 13 (the gradients):
+//     dV   += P_i^T dO_i   A = P^T from TMEM, after P_i^T is stored       -> DVDONE
+//     dQ_i  = dS_i K       after dS_i^T is in smem (dP^T_i read)          -> DQFULL
+//     dK   += dS_i^T Q_i                                                   -> DSCONS, QEMPTY
 // MMAs into different accumulators are not ordered by the hardware, so every
 // reuse of a TMEM region or smem buffer waits for a commit of its readers.
 // The dQ partial of each query tile leaves TMEM through shared memory and is
@@ -231,7 +229,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::B_DQFULL), 1);
     mbar_init(bar(L::B_DQFREE), 128);
     mbar_init(bar(L::B_DSCONS), 1);
-    mbar_init(bar(L::B_ACC), 1);
+    mbar_init(bar(L::B_ACC), 2);  // one commit from each MMA issuer
     fence_mbar_init();
   }
   if (warp == 13) {
@@ -340,8 +338,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (st == 0) ++nq0; else ++nq1;
           }
           if (i + 1 < n_iter) fetch(i + 1);
-          // dO has one buffer: tile i's once dV of tile i-1 has read it
-          if (i >= 1 && !mbar_wait_warp(wc, bar(L::B_DVDONE), uint32_t(i - 1) & 1u)) {
+          // dO has one buffer: tile i's once dV and dP^T of tile i-1 have read it
+          // (two threads issue them, so neither commit covers the other)
+          if (i >= 1 && !mbar_wait2_warp(wc, bar(L::B_DVDONE), uint32_t(i - 1) & 1u, bar(L::B_DPFULL),
+                                         uint32_t(i - 1) & 1u)) {
             ok = false;
             break;
           }
@@ -362,15 +362,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     } else if (warp == 13 || warp == 14) {
       // ----------------------------------------------------------------- MMA
-      // Warp 9 issues every MMA (lane 0); warp 10 waits on the mbarriers each
-      // product depends on and opens a named-barrier gate for it.  An mbarrier
-      // wait issued right behind a batch of MMAs queues behind them (hundreds
-      // of cycles even on a completed phase), while a named barrier costs a
-      // few cycles, so the issuing warp only ever meets named barriers.  The
-      // gate also carries the waiter's verdict: a failed wait stops both warps
-      // at the same gate.
-      const bool issuer = warp == 13;
-      auto gate = [&](bool wait_ok) -> bool { return named_bar_and(kMmaGate, 64, wait_ok); };
+      // Two issuers, each waiting on the mbarriers of its own products: warp
+      // 14 issues what the P/dS warps consume (S^T, dP^T), warp 13 the
+      // gradients (dV, dQ, dK), lane 0 each.  A tcgen05.mma holds its issuing
+      // thread until the pipe accepts it, so a single issuer queued every
+      // product behind the issue of the one before.  The two meet only through
+      // mbarriers: the next S^T waits for dV to have read P^T out of its
+      // columns, the next dP^T for the dQ read-out, dQ for dS^T (which also
+      // means dP^T was read).  Each commit tracks its own thread's MMAs.
+      const bool score_issuer = warp == 14;
       auto wt = [&](int b, uint32_t parity) -> bool { return mbar_wait_warp(wc, bar(b), parity); };
       auto wt2 = [&](int b1, uint32_t p1, int b2, uint32_t p2) -> bool {
         return mbar_wait2_warp(wc, bar(b1), p1, bar(b2), p2);
@@ -402,23 +402,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mma_commit(bar(L::B_DPFULL));
       };
+      bool go = true;
       if (n_iter > 0) {
-        bool go = gate(issuer || wt2(L::B_KV, 0, L::B_QFULL, 0));
-        if (go && issuer) {
-          tc_fence_after();
-          if (lane == 0) issue_s(0);
-        }
-        go = go && gate(issuer || wt(L::B_DOFULL, 0));
-        if (go && issuer) {
-          tc_fence_after();
-          if (lane == 0) issue_dp();
-        }
-        for (int i = 0; go && i < n_iter; ++i) {
-          const uint32_t ph = uint32_t(i) & 1u;
-          const int st = i & 1;
-          // dV += P^T dO, P^T (bf16 pairs) in the S^T columns
-          if (!(go = gate(issuer || wt(L::B_PFULL, ph)))) break;
-          if (issuer) {
+        if (score_issuer) {
+          for (int i = 0; go && i < n_iter; ++i) {
+            const uint32_t ph = uint32_t(i) & 1u;
+            // S_i^T once Q_i is in and dV_{i-1} has read P^T out of the S^T columns
+            if (!(go = i == 0 ? wt2(L::B_KV, 0, L::B_QFULL, 0)
+                              : wt2(L::B_QFULL + (i & 1), uint32_t(i >> 1) & 1u, L::B_DVDONE, ph ^ 1u)))
+              break;
+            tc_fence_after();
+            if (lane == 0) issue_s(i);
+            // dP_i^T once dO_i is in and dQ_{i-1} has left the dP^T columns
+            if (!(go = i == 0 ? wt(L::B_DOFULL, 0) : wt2(L::B_DOFULL, ph, L::B_DQFREE, ph ^ 1u)))
+              break;
+            tc_fence_after();
+            if (lane == 0) issue_dp();
+          }
+        } else {
+          for (int i = 0; go && i < n_iter; ++i) {
+            const uint32_t ph = uint32_t(i) & 1u;
+            const int st = i & 1;
+            // dV += P^T dO, P^T (bf16 pairs) in the S^T columns, once dO_i landed
+            // (the other issuer's dP^T_i no longer stands between them)
+            if (!(go = wt2(L::B_PFULL, ph, L::B_DOFULL, ph))) break;
             tc_fence_after();
             if (lane == 0) {
               const uint32_t ol = opaque(sdesc_lo(base + L::DO, L::CHUNK));
@@ -429,11 +436,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                sdesc_of_lo(ol + ((2048u * kk) >> 4)), idAcc);
               mma_commit(bar(L::B_DVDONE));
             }
-          }
-          // dQ = dS K right behind dV, so the wait of the next S^T for dV to
-          // complete overlaps it
-          if (!(go = gate(issuer || wt(L::B_DSFULL, ph)))) break;
-          if (issuer) {
+            // dQ = dS K into the dP^T columns, then dK += dS^T Q
+            if (!(go = wt(L::B_DSFULL, ph))) break;
             tc_fence_after();
             if (lane == 0) {
               const uint32_t sl = opaque(sdesc_lo(base + L::DS, L::CHUNK));
@@ -444,22 +448,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_ss_c<true>(tbase + kColDP, sdesc_of_lo(sl + ((2048u * kk) >> 4)),
                                sdesc_of_lo(kl + ((2048u * kk) >> 4)), idDQ);
               mma_commit(bar(L::B_DQFULL));
-            }
-          }
-          // next S^T once its Q is in and dV has read P^T out of the S^T columns
-          if (i + 1 < n_iter) {
-            if (!(go = gate(issuer || wt2(L::B_QFULL + (st ^ 1), uint32_t((i + 1) >> 1) & 1u,
-                                          L::B_DVDONE, ph))))
-              break;
-            if (issuer) {
-              tc_fence_after();
-              if (lane == 0) issue_s(i + 1);
-            }
-          }
-          // dK += dS^T Q (dS^T is already in: its gate opened for dQ)
-          if (issuer) {
-            tc_fence_after();
-            if (lane == 0) {
               const uint32_t tl = opaque(sdesc_lo(base + L::DS, 16));
               const uint32_t ql = opaque(sdesc_lo(base + L::Q + st * L::TILE, L::CHUNK));
               mma_ss(tbase + kColDK, sdesc_of_lo(tl), sdesc_of_lo(ql), idAcc, i > 0 ? 1u : 0u);
@@ -473,18 +461,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_commit(bar(L::B_QEMPTY + st));
             }
           }
-          // next dP^T once dQ has left the dP^T columns and dO_{i+1} is in
-          if (i + 1 < n_iter) {
-            if (!(go = gate(issuer || wt2(L::B_DOFULL, uint32_t(i + 1) & 1u, L::B_DQFREE, ph))))
-              break;
-            if (issuer) {
-              tc_fence_after();
-              if (lane == 0) issue_dp();
-            }
-          }
         }
         ok = go;
-        if (issuer && lane == 0) {
+        if (lane == 0) {
+          // The accumulator barrier takes one commit from each issuer: every
+          // MMA has completed once it flips.
           mma_commit(bar(L::B_ACC));
           drain_wait(wc, bar(L::B_ACC), 0);
         }
