@@ -24,9 +24,10 @@
 // value) in the swizzled layout the MMA reads, and the scales are applied in
 // fp32: S = k_scale * (Q K8^T), O = v_scale * (P V8).
 //
-// Roles (192 threads): warps 0..3 expand FP8 tiles, run the softmax (thread r
+// Roles (224 threads): warps 0..3 expand FP8 tiles, run the softmax (thread r
 // owns TMEM lane r = query row r) and the epilogue; warp 4 issues the TMA
-// loads; warp 5 allocates TMEM and issues the MMAs (one thread).
+// loads; warp 5 allocates TMEM and issues the S products, warp 6 the P V
+// products (one thread each).
 // TMEM columns: S [0,128)  O [128,128+D)  P [128+D,192+D).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -38,7 +39,7 @@
 namespace bda {
 namespace {
 
-constexpr int kDecThreads = 192;
+constexpr int kDecThreads = 224;
 constexpr uint32_t kColS = 0, kColO = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the persistent forward
 
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     mbar_init(bar(L::B_SFREE), 128);
     mbar_init(bar(L::B_PF), 128);
     mbar_init(bar(L::B_OD), 1);
-    mbar_init(bar(L::B_DRAIN), 1);
+    mbar_init(bar(L::B_DRAIN), 2);  // one commit from each MMA issuer
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -244,8 +245,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 5 || warp == 6) {
     // ----------------------------------------------------------------- MMA
+    // Two issuers, each waiting on the mbarriers of its own products: warp 5
+    // issues every S, warp 6 every P V (lane 0 each).  A tcgen05.mma holds its
+    // issuing thread until the pipe accepts it, and with one issuer a P V
+    // waited behind the wait for the next tile's K.  The products share no
+    // operand (S and P have buffers of their own, K and V stages too) and each
+    // commit tracks its own thread's MMAs.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
@@ -273,35 +280,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         mma_commit(bar(L::B_OD));
         mma_commit(bar(L::B_VE + s));
       };
-      bool go = mbar_wait(wc, bar(L::B_Q), 0);
-      // S(j) waits for its K and for the softmax to have read S(j-1); P V(j-1)
-      // is issued behind S(j), so the product overlaps the next softmax.
-      for (int j = 0; go && j < n; ++j) {
-        const int s = j & 1;
-        go = mbar_wait(wc, bar(b_kready + s), uint32_t(j >> 1) & 1u) &&
-             (j == 0 || mbar_wait(wc, bar(L::B_SFREE), uint32_t(j - 1) & 1u));
-        if (!go) break;
-        tc_fence_after();
-        issue_s(j);
-        if (j > 0) {
-          const int sp = (j - 1) & 1;
-          go = mbar_wait(wc, bar(L::B_PF), uint32_t(j - 1) & 1u) &&
-               mbar_wait(wc, bar(b_vready + sp), uint32_t((j - 1) >> 1) & 1u);
+      if (warp == 5) {
+        // S(j) once Q and its K are in and the softmax has read S(j-1)
+        bool go = mbar_wait(wc, bar(L::B_Q), 0);
+        for (int j = 0; go && j < n; ++j) {
+          const int s = j & 1;
+          go = mbar_wait(wc, bar(b_kready + s), uint32_t(j >> 1) & 1u) &&
+               (j == 0 || mbar_wait(wc, bar(L::B_SFREE), uint32_t(j - 1) & 1u));
           if (!go) break;
           tc_fence_after();
-          issue_pv(j - 1);
+          issue_s(j);
         }
-      }
-      if (go) {
-        const int jl = n - 1, sl = jl & 1;
-        go = mbar_wait(wc, bar(L::B_PF), uint32_t(jl) & 1u) &&
-             mbar_wait(wc, bar(b_vready + sl), uint32_t(jl >> 1) & 1u);
-        if (go) {
+      } else {
+        // P V(j) once P(j) is out and its V is in
+        for (int j = 0; j < n; ++j) {
+          const int s = j & 1;
+          if (!(mbar_wait(wc, bar(L::B_PF), uint32_t(j) & 1u) &&
+                mbar_wait(wc, bar(b_vready + s), uint32_t(j >> 1) & 1u)))
+            break;
           tc_fence_after();
-          issue_pv(jl);
+          issue_pv(j);
         }
       }
-      // Every MMA issued above completes before TMEM can be released.
+      // Every MMA issued above completes before TMEM can be released (the
+      // drain barrier takes one commit from each issuer).
       mma_commit(bar(L::B_DRAIN));
       drain_wait(wc, bar(L::B_DRAIN), 0);
     }
